@@ -1,0 +1,355 @@
+"""Benchmark of the tree-masked attention hot path on GB300.
+
+One step = the whole path over one tree: plan (host node pass + device kernels), RoPE at
+depth positions, attention forward, the g_t/K loss weights on the upstream gradient, and
+the backward (delta, dK/dV with on-chip reduction and the dQ accumulator, dQ finalize).
+Inputs are resident in HBM before the timed region; the L2 (129 MB) is flushed by writing a
+256 MiB buffer between steps, outside the CUDA-event brackets.
+
+Metric: visible-pair TFLOP/s = 14 d Hq N_pairs / step time (forward 4 d, backward 10 d flops
+per visible query-key pair per q head; N_pairs = sum_t (pos_t + 1)), plus tokens/s.
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+Under torchrun each rank runs its own tree (weak scaling, no data-path collective); rank 0
+prints one JSON line with the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import CONFIGS, make_tensors, make_workload  # noqa: E402
+
+METRIC = "tree-attn fwd+bwd visible-pair TFLOP/s and tokens/s on 1 GB300; % of bf16 peak"
+UNIT = "TFLOP/s"
+DEFAULT_CONFIG = "rollout32k"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return dict(bf16=float(d["bf16_tflops"]), bf16_sustained=float(d.get("bf16_tflops_sustained", 0)) or None,
+                    hbm=float(d["hbm_gbs"]), source="measured")
+    return dict(bf16=1900.0, bf16_sustained=1700.0, hbm=6800.0, source="fallback")
+
+
+def host_stats(parent, node_len):
+    """N, K, N_pairs and N_flat from parent pointers (plain host loops, no oracle import)."""
+    n = len(parent)
+    depth_off = np.zeros(n, dtype=np.int64)
+    leaves = np.zeros(n, dtype=np.int64)
+    has_child = np.zeros(n, dtype=bool)
+    for c in range(n):                                  # parents precede children in these trees
+        if parent[c] >= 0:
+            has_child[parent[c]] = True
+    order = sorted(range(n), key=lambda v: _depth(parent, v))
+    for v in order:
+        if parent[v] >= 0:
+            depth_off[v] = depth_off[parent[v]] + node_len[parent[v]]
+    for leaf in np.nonzero(~has_child)[0]:
+        v = leaf
+        while v >= 0:
+            leaves[v] += 1
+            v = parent[v]
+    L = node_len.astype(np.int64)
+    n_pairs = int((L * depth_off + L * (L + 1) // 2).sum())
+    N = int(L.sum())
+    return dict(N=N, K=int((~has_child).sum()), n_pairs=n_pairs, n_flat=int((L * leaves).sum()))
+
+
+def _depth(parent, v):
+    d = 0
+    while parent[v] >= 0:
+        v = parent[v]
+        d += 1
+    return d
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling every 200 ms while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            for line in open(self.path):
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 8:
+                    rows.append(parts)
+        except OSError:
+            pass
+        finally:
+            try:
+                os.unlink(self.path)
+            except OSError:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower() == "active"})
+        under = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        return {"sm_mhz": float(np.median(under)) if under else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def run_ours(args, rank, world, dev):
+    import tree_masked_attention_plan_gb300 as tam
+    torch.cuda.set_device(dev)
+    wl = make_workload(args.config)
+    st = host_stats(wl.parent, wl.node_len)
+    t = make_tensors(wl)
+    Hq, Hkv, d, N = wl.Hq, wl.Hkv, wl.d, st["N"]
+    stream = torch.cuda.current_stream()
+    q, k, v, u = (t[x].to(dev) for x in ("q", "k", "v", "u"))
+    status = tam.new_status(dev)
+    plan = tam.tree_plan(wl.parent, wl.node_len, device=dev)
+    Np = plan.n_pad
+    qr, kr = torch.empty_like(q), torch.empty_like(k)
+    o = torch.empty_like(q)
+    lse = torch.empty(Hq, Np, dtype=torch.float32, device=dev)
+    dO = torch.empty_like(u)
+    ws = torch.empty(tam.tree_attn_bwd_workspace(plan, Hq, d), dtype=torch.uint8, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    ev = {n: [torch.cuda.Event(enable_timing=True) for _ in range(2)] for n in ("step", "fwd")}
+    bwd_ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    theta = wl.theta
+
+    def step(p):
+        tam.tree_rope_fwd(p, q, k, theta, qr=qr, kr=kr)
+        ev["fwd"][0].record(stream)
+        tam.tree_attn_fwd(p, qr, kr, v, o=o, lse=lse, status=status)
+        ev["fwd"][1].record(stream)
+        tam.tree_apply_weights(p, u, out=dO)
+        tam.tree_attn_bwd(p, qr, kr, v, o, lse, dO, rope_theta=theta, workspace=ws, dq=dq, dk=dk, dv=dv,
+                          status=status)
+
+    def full_step():
+        ev["step"][0].record(stream)
+        p = tam.tree_plan(wl.parent, wl.node_len, device=dev)
+        step(p)
+        ev["step"][1].record(stream)
+        return p
+
+    tam.tree_set_timing_events(bwd_ev)
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        full_step()
+    torch.cuda.synchronize()
+    tam.check_status(status, "warmup")
+    times = {"step": [], "fwd": [], "bwd": [], "dkdv": []}
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        wall0 = time.perf_counter()
+        for _ in range(args.steps):
+            flush.fill_(1.0)
+            full_step()
+            torch.cuda.synchronize()
+            times["step"].append(ev["step"][0].elapsed_time(ev["step"][1]))
+            times["fwd"].append(ev["fwd"][0].elapsed_time(ev["fwd"][1]))
+            times["bwd"].append(bwd_ev[0].elapsed_time(bwd_ev[3]))
+            times["dkdv"].append(bwd_ev[1].elapsed_time(bwd_ev[2]))
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    if world > 1:
+        torch.distributed.barrier()
+    tam.tree_set_timing_events([])
+    tam.check_status(status, "timed steps")
+    clocks = clk.summary()
+
+    # e2e: the same step through the public API from pinned host buffers, copies inside
+    hq, hk, hv, hu = (t[x].pin_memory() for x in ("q", "k", "v", "u"))
+    ho, hdq, hdk, hdv = (torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (o, dq, dk, dv))
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hu)) + 8 * len(wl.parent)
+    d2h = sum(x.numel() * x.element_size() for x in (ho, hdq, hdk, hdv))
+    e2e_ms = []
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for it in range(args.warmup + args.steps):
+        flush.fill_(1.0)
+        e0.record(stream)
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        u.copy_(hu, non_blocking=True)
+        full_step()
+        ho.copy_(o, non_blocking=True)
+        hdq.copy_(dq, non_blocking=True)
+        hdk.copy_(dk, non_blocking=True)
+        hdv.copy_(dv, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if it >= args.warmup:
+            e2e_ms.append(e0.elapsed_time(e1))
+    tam.check_status(status, "e2e steps")
+
+    res = dict(st=st, wl=wl, times=times, wall=wall, clocks=clocks, e2e_ms=float(np.mean(e2e_ms)), h2d=h2d, d2h=d2h,
+               nnz=int(plan.arrays()["counts"][0].item()))
+    return res
+
+
+def cpu_baseline_sample(config, budget_s=20.0):
+    """The oracle as it stands, on the host cores: path-expanded fp64 attention fwd+bwd for q head 0
+    over a prefix of the root-to-leaf paths that fits the time budget.  Credit: 14 d times the
+    visible pairs the sampled paths compute (each path is its own causal sequence)."""
+    import oracle
+    wl = make_workload(config)
+    t = make_tensors(wl)
+    p = oracle.plan(wl.parent, wl.node_len)
+    done_pairs, t0, n_paths = 0, time.perf_counter(), 0
+    sub = dict(p)
+    for path in p["paths"]:
+        sub["paths"] = [path]
+        sub["n_paths"] = p["n_paths"]
+        L = int(sum(wl.node_len[x] for x in path))
+        oracle.attention_paths(wl.parent, wl.node_len, t["q"][:, :1], t["k"][:, :1], t["v"][:, :1], t["u"][:, :1],
+                               heads=[0], p=sub, theta=wl.theta)
+        done_pairs += L * (L + 1) // 2
+        n_paths += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    el = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return dict(value=14 * wl.d * done_pairs / el / 1e12, unit=UNIT, cores=cores, kind="oracle",
+                sample=f"{config}: fp64 path-expanded fwd+bwd, q head 0, first {n_paths} of {p['n_paths']} "
+                       f"root-to-leaf paths ({done_pairs} causal pairs), {el:.1f} s; NumPy/BLAS default threads",
+                seconds=el)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=list(CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        return run_reference(args)
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    res = run_ours(args, rank, world, dev)
+    st, wl, times = res["st"], res["wl"], res["times"]
+    ms = float(np.mean(times["step"]))
+    ms_fwd, ms_bwd, ms_dkdv = (float(np.mean(times[x])) for x in ("fwd", "bwd", "dkdv"))
+    ms_t = torch.tensor([ms, res["e2e_ms"]], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(ms_t, op=torch.distributed.ReduceOp.MAX)
+    ms_max, e2e_max = float(ms_t[0]), float(ms_t[1])
+    flops = 14.0 * wl.d * wl.Hq * st["n_pairs"]
+    peaks = load_peaks()
+    value = world * flops / (ms_max * 1e-3) / 1e12
+    dkdv_flops = 10.0 * wl.d * wl.Hq * st["n_pairs"]
+    achieved = dkdv_flops / (ms_dkdv * 1e-3) / 1e12
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded tree and N(0,1) bf16 tensors)",
+            "config": {"workload": wl.name, "N": st["N"], "paths_K": st["K"], "N_pairs": st["n_pairs"],
+                       "N_flat": st["n_flat"], "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d, "rope_theta": wl.theta,
+                       "nonempty_tiles": res["nnz"], "step": "plan+rope+fwd+weights+bwd",
+                       "l2": "flushed between steps (256 MiB write, outside the event brackets)",
+                       "parallelism": f"one tree per rank x{world}"},
+            "tokens_per_s": round(world * st["N"] / (ms_max * 1e-3), 1),
+            "pct_bf16_peak": round(100 * value / world / peaks["bf16"], 2),
+            "breakdown_ms": {"step": round(ms, 4), "fwd": round(ms_fwd, 4), "bwd": round(ms_bwd, 4),
+                             "bwd_dkdv": round(ms_dkdv, 4),
+                             "attention_fwd_bwd_tflops": round(flops / ((ms_fwd + ms_bwd) * 1e-3) / 1e12, 2)},
+            "e2e": {"value": round(world * flops / (e2e_max * 1e-3) / 1e12, 2), "unit": UNIT,
+                    "ms_per_step": round(e2e_max, 4), "h2d_bytes_per_step": res["h2d"],
+                    "d2h_bytes_per_step": res["d2h"]},
+            "roofline": {"kernel": "k_bwd_dkdv", "bound": "tensor", "achieved": round(achieved, 2),
+                         "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16"], 4),
+                         "peak_source": f"{peaks['source']} bf16 burst", "traffic": None,
+                         "algorithmic": "10 d Hq N_pairs flops per launch"},
+            "gpu_launches": 14 * args.steps,
+            "clocks": res["clocks"],
+            "wall_s_timed_region": round(res["wall"], 3),
+        }
+        if not args.no_cpu_baseline:
+            cb = cpu_baseline_sample(args.config, budget_s=15.0)
+            cb.pop("seconds", None)
+            line["cpu_baseline"] = cb
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle (the only reference implementation there is), each step a
+    bounded sample of the same workload, on the host cores."""
+    res = []
+    for i in range(args.warmup + args.steps):
+        cb = cpu_baseline_sample(args.config, budget_s=4.0)
+        if i >= args.warmup:
+            res.append(cb)
+    value = float(np.mean([r["value"] for r in res]))
+    secs = float(np.mean([r["seconds"] for r in res]))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs * 1e3, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded tree and N(0,1) bf16 tensors)",
+            "config": {"workload": args.config, "parallelism": "host cores, rank 0 only"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": res[0]["cores"], "kind": "oracle",
+                             "sample": res[0]["sample"]},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,197 @@
+/*
+ * tree_attn.h - C ABI of the GB300 (sm_103a) tree-masked attention library.
+ *
+ * What it computes (all citations are to "Tree Training 技术详解", tingdeliu.github.io):
+ *   A prefix tree of token segments (section 3.1) is packed depth-first, each node's tokens
+ *   once (section 3.2, X_DFS).  Token i may attend to token j iff j <= i and node(j) is
+ *   node(i) or an ancestor of it (section 4.2, mask M_ij), tested here in interval form
+ *   dfs_in(node j) <= dfs_in(node i) <= dfs_out(node j) (section 4.3: node DFS intervals).
+ *   RoPE positions follow tree depth (section 5); g_t counts the root-to-leaf paths through
+ *   token t and g_t/K is its loss weight (section 6.2).
+ *
+ * Conventions shared by every entry point
+ *   - Every function returns int status: TREE_OK (0) or a negative TREE_ERR_* code.  No C++
+ *     exception crosses this boundary.  tree_strerror() names a code; after TREE_ERR_CUDA,
+ *     tree_last_cuda_error() gives the CUDA runtime's message for the calling thread.
+ *   - Device pointers are caller-owned (for example allocated by PyTorch).  The library
+ *     never allocates or frees device memory and never synchronizes a stream.  The one host
+ *     to device copy it makes is inside tree_plan(), ordered on the given stream.
+ *   - Launches are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *     Errors found on the device (a bounded wait that expired) are written to the int32
+ *     `status_dev` word that the caller passes and reads back after synchronizing; the
+ *     kernels only ever store a nonzero code there, so the caller zeroes it beforehand.
+ *   - Tensors are bf16 (raw 16-bit words, tree_bf16), row-major, token-major: Q, O, dO, dQ
+ *     are [N][Hq][d]; K, V, dK, dV are [N][Hkv][d], tokens in packed depth-first order
+ *     (node order[0]'s tokens first; node v's tokens start at tok_start[v]).  Pointers to
+ *     them must be 16-byte aligned.  Head dimension d is 64 or 128; Hq % Hkv == 0 and
+ *     q head h reads kv head h / (Hq / Hkv).
+ *   - N_pad = n_tiles * 128.  Per-token plan arrays and the LSE rows are N_pad long; the
+ *     entries past N are padding that the library writes itself.
+ *   - Only compute capability 10.3 (GB300) is accepted: TREE_ERR_ARCH otherwise.
+ */
+#ifndef TREE_ATTN_H
+#define TREE_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t tree_bf16;             /* bfloat16 bit pattern */
+typedef struct CUstream_st* tree_stream_t; /* identical to cudaStream_t */
+
+#define TREE_TILE 128                   /* query and key tile edge */
+
+enum {
+  TREE_OK = 0,
+  TREE_ERR_INVALID_TREE = -1, /* parent out of range, self parent, cycle, no root,
+                                 node_len < 0, token total 0 or > 2^31-1 */
+  TREE_ERR_SHAPE = -2,        /* d not 64/128, Hq % Hkv != 0, non-positive heads, plan mismatch */
+  TREE_ERR_ARCH = -3,         /* current device is not compute capability 10.3 */
+  TREE_ERR_CUDA = -4,         /* a CUDA runtime call or launch failed */
+  TREE_ERR_TIMEOUT = -5,      /* a bounded device wait expired (written to status_dev) */
+  TREE_ERR_ARG = -6           /* NULL or misaligned pointer, bad size */
+};
+
+/* ---------------------------------------------------------------------------------------
+ * Plan
+ * -------------------------------------------------------------------------------------*/
+
+typedef struct {
+  int32_t n_nodes;    /* nodes in the tree */
+  int32_t n_tokens;   /* N = sum of node lengths */
+  int32_t n_tiles;    /* T = ceil(N / 128) */
+  int32_t n_paths;    /* K = root-to-leaf paths (leaves of all roots) */
+  int64_t max_nnz;    /* T (T + 1) / 2: capacity of row_idx / col_idx */
+  int64_t plan_bytes; /* device bytes tree_plan_bind() carves the plan arrays from */
+} tree_plan_info;
+
+/* Host-side descriptor of a plan; every pointer is device memory inside the buffer given
+ * to tree_plan_bind().  Per-node arrays are indexed by node id unless noted. */
+typedef struct {
+  /* per node [n_nodes] */
+  int32_t* order;         /* depth-first preorder of node ids (children by ascending id) */
+  int32_t* dfs_in;        /* preorder index of the node */
+  int32_t* dfs_out;       /* preorder index of the last node of its subtree (inclusive) */
+  int32_t* tok_start;     /* first packed token of the node */
+  int32_t* depth_off;     /* sum of the ancestors' lengths = position of its first token */
+  int32_t* leaves;        /* root-to-leaf paths through the node (g of its tokens) */
+  int32_t* dfs_tok_start; /* tok_start indexed by preorder index */
+  int32_t* sub_end;       /* one past the last packed token of the node's subtree */
+  /* per packed token [N_pad]; entries >= N are padding */
+  int32_t* tok_node;      /* node id of the token (pad: -1) */
+  int32_t* pos;           /* RoPE position = depth_off + offset in node (pad: 0) */
+  int32_t* g;             /* path count g_t (pad: 0) */
+  int32_t* tok_in;        /* dfs_in of the token's node (pad: -1) */
+  int32_t* tok_out;       /* dfs_out of the token's node (pad: -2) */
+  int32_t* hi;            /* sub_end(node) - 1: last token that can see this one (pad: -1) */
+  float* w;               /* g_t / K, IEEE fp32 round-to-nearest division (pad: 0) */
+  /* tile table, tiles are 128 x 128: query tile qt (rows), key tile kt (columns) */
+  uint8_t* tile_class;    /* [T*T] row-major [qt][kt]: 0 empty, 1 partial, 2 full */
+  int32_t* row_ptr;       /* [T+1] CSR over query tiles */
+  int32_t* row_idx;       /* [max_nnz] non-empty kt of each qt, ascending */
+  int32_t* col_ptr;       /* [T+1] CSR over key tiles */
+  int32_t* col_idx;       /* [max_nnz] non-empty qt of each kt, ascending */
+  int32_t* row_order;     /* [T] query tiles by descending row count (ties: ascending) */
+  int32_t* col_order;     /* [T] key tiles by descending column count (ties: ascending) */
+  int32_t* tile_hi_min;   /* [T] min of hi over the key tile's real tokens */
+  int32_t* tile_hi_max;   /* [T] max of hi over the key tile's real tokens */
+  int32_t* counts;        /* [4] nnz, n_full, n_partial, reserved (0) */
+  int32_t n_nodes, n_tokens, n_tiles, n_paths;
+} tree_plan_t;
+
+/* Validate the tree and report its sizes.  Host only, no CUDA call.
+ * parent[i] is the parent id of node i (-1 for a root); node_len[i] >= 0 its token count.
+ * Returns TREE_ERR_INVALID_TREE on any of the conditions listed with that code. */
+int tree_plan_query(const int32_t* parent, const int32_t* node_len, int32_t n_nodes,
+                    tree_plan_info* info);
+
+/* Carve the plan arrays out of a caller-owned device buffer of info->plan_bytes bytes
+ * (256-byte aligned) and fill `plan`'s pointers and sizes.  Host only, no CUDA call. */
+int tree_plan_bind(const tree_plan_info* info, void* device_buffer, tree_plan_t* plan);
+
+/* Build the plan on `stream` (sections 3.2, 4.3, 5, 6.2 of the explainer):
+ *   host:   validation, depth-first preorder (children by ascending id), dfs_in/dfs_out,
+ *           tok_start, depth_off, leaves, sub_end; one async copy of these to the device;
+ *   device: per-token expansion (tok_node, pos, g, w, tok_in, tok_out, hi), per-key-tile
+ *           hi range, tile classes, row/column CSR lists and heaviest-first orders.
+ * `plan` must come from tree_plan_bind() for the same tree.  The host arrays may be freed
+ * when the call returns. */
+int tree_plan(const int32_t* parent, const int32_t* node_len, int32_t n_nodes,
+              const tree_plan_t* plan, tree_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * RoPE and loss weights
+ * -------------------------------------------------------------------------------------*/
+
+/* Rotate-half RoPE at the plan's depth positions (section 5): for c < d/2,
+ * angle = pos * theta^(-2c/d) in fp32, x'_c = x_c cos - x_{c+d/2} sin,
+ * x'_{c+d/2} = x_{c+d/2} cos + x_c sin.  q -> qr [N][Hq][d], k -> kr [N][Hkv][d];
+ * in place (qr == q, kr == k) is allowed. */
+int tree_rope_fwd(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k,
+                  tree_bf16* qr, tree_bf16* kr, int Hq, int Hkv, int d, float theta,
+                  tree_stream_t stream);
+
+/* dO_t = (g_t / K) * U_t (section 6.2: the per-token weight of the tree loss), u and dO
+ * [N][H][d] bf16; in place allowed. */
+int tree_apply_weights(const tree_plan_t* plan, const tree_bf16* u, tree_bf16* dO, int H,
+                       int d, tree_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Attention (section 4.2: Softmax(Q K^T / sqrt(d) + M) V, block-sparse per section 4.3)
+ * -------------------------------------------------------------------------------------*/
+
+/* Forward.  q, k: RoPE-rotated inputs; v.  Writes o [N][Hq][d] bf16 and
+ * lse [Hq][N_pad] fp32 = natural log of sum_j exp(scale q_i.k_j) over visible j
+ * (padding entries 0).  scale <= 0 selects 1/sqrt(d).  Only non-empty tiles are
+ * computed; the mask is evaluated on partial tiles only. */
+int tree_attn_fwd(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k,
+                  const tree_bf16* v, int Hq, int Hkv, int d, float scale, tree_bf16* o,
+                  float* lse, int32_t* status_dev, tree_stream_t stream);
+
+/* Bytes of device workspace tree_attn_bwd needs: delta [Hq][N_pad] fp32 followed by the
+ * fp32 dQ accumulator [Hq][d][N_pad]. */
+size_t tree_attn_bwd_workspace(const tree_plan_t* plan, int Hq, int d);
+
+/* Backward of tree_attn_fwd (section 6.2: gradients of shared ancestors add up).
+ * Inputs as in the forward plus o, lse and dO = dL/dO [N][Hq][d].  Outputs dq [N][Hq][d],
+ * dk, dv [N][Hkv][d] bf16.  With rope_theta > 0 the inverse RoPE rotation at the plan's
+ * positions is applied to dq and dk, so they are gradients w.r.t. the un-rotated q, k;
+ * rope_theta <= 0 returns gradients w.r.t. the rotated inputs.  dK and dV are reduced
+ * on chip per key tile and written once.  `workspace` holds tree_attn_bwd_workspace()
+ * bytes, 256-byte aligned; its contents need not be initialised. */
+int tree_attn_bwd(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k,
+                  const tree_bf16* v, const tree_bf16* o, const float* lse,
+                  const tree_bf16* dO, int Hq, int Hkv, int d, float scale, float rope_theta,
+                  void* workspace, tree_bf16* dq, tree_bf16* dk, tree_bf16* dv,
+                  int32_t* status_dev, tree_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Diagnostics
+ * -------------------------------------------------------------------------------------*/
+
+/* Device waits give up after this many nanoseconds and report TREE_ERR_TIMEOUT
+ * (default 2e9).  Values < 1e5 are raised to 1e5.  Process-wide. */
+int tree_set_wait_limit_ns(int64_t ns);
+
+/* Launch one kernel that waits on a barrier nobody arrives at, with a limit of `ns`
+ * nanoseconds; it must store TREE_ERR_TIMEOUT into *status_dev and exit normally.
+ * Exercises the bounded-wait path without faulting or hanging the GPU. */
+int tree_selftest_timeout(int32_t* status_dev, int64_t ns, tree_stream_t stream);
+
+/* Register up to 4 cudaEvent_t handles (created by the caller on the current device) that
+ * tree_attn_bwd records on its stream: [0] before the delta/zeroing kernels, [1] before the
+ * dK/dV kernel, [2] after it, [3] after the dQ finalize kernel.  n = 0 unregisters.  For
+ * per-kernel timing with CUDA events; process-wide, not thread-safe. */
+int tree_set_timing_events(void* const* events, int n);
+
+const char* tree_strerror(int code);
+const char* tree_last_cuda_error(void);
+int tree_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TREE_ATTN_H */

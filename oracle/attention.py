@@ -132,7 +132,7 @@ def attention_paths(parent, node_len, q, k, v, u, scale=None, theta=10000.0, hea
 
 
 def attention_nodes(parent, node_len, q, k, v, u, scale=None, theta=10000.0, heads=None,
-                    use_rope=True, p=None, row_chunk=2048):
+                    use_rope=True, p=None, row_chunk=2048, nodes=None):
     """The same result written with the tree mask of section 4.2 instead of path expansion.
 
     For each node a, its tokens are the queries; the keys are the tokens of a's ancestors
@@ -141,6 +141,8 @@ def attention_nodes(parent, node_len, q, k, v, u, scale=None, theta=10000.0, hea
     counted from the paths.  Nothing is shared between nodes except the summed gradients.
     Rows of a long node are taken `row_chunk` at a time; each chunk is the full row set of
     those queries, so the result does not depend on the chunk size.
+    With `nodes` given, only those nodes' tokens act as queries: their O, LSE and dQ are exact,
+    and so are dK, dV of every key that no other node's tokens can see (e.g. a leaf's own keys).
     """
     q, k, v, u = _f64(q), _f64(k), _f64(v), _f64(u)
     N, Hq, d = q.shape
@@ -161,7 +163,7 @@ def attention_nodes(parent, node_len, q, k, v, u, scale=None, theta=10000.0, hea
     dK = np.zeros((N, Hkv, d))
     dV = np.zeros((N, Hkv, d))
     for a, path in chain.items():
-        if nl[a] == 0:
+        if nl[a] == 0 or (nodes is not None and a not in nodes):
             continue
         kidx = np.concatenate([np.arange(p["tok_start"][b], p["tok_start"][b] + nl[b])
                                for b in path]).astype(np.int64)

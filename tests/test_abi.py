@@ -1,0 +1,105 @@
+"""CPU-side checks of the C ABI: the library builds, loads without a GPU, exports every entry
+point include/tree_attn.h declares, and its host-only functions validate trees."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import tree_masked_attention_plan_gb300 as tam
+from workloads import CONFIGS, make_workload, random_tree
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(tam.LIB_PATH):
+        from tree_masked_attention_plan_gb300 import build_lib
+        build_lib.build()
+    return ctypes.CDLL(tam.LIB_PATH)
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "tree_attn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\*?\s+\**(tree_[a-z_0-9]+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for n in ("tree_plan_query", "tree_plan_bind", "tree_plan", "tree_rope_fwd", "tree_attn_fwd",
+              "tree_attn_bwd", "tree_attn_bwd_workspace", "tree_strerror"):
+        assert n in names
+
+
+def test_every_declared_symbol_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_plan_query_sizes_match_oracle(lib):
+    for name in CONFIGS:
+        wl = make_workload(name)
+        info = tam.tree_plan_query(wl.parent, wl.node_len)
+        p = oracle.plan(wl.parent, wl.node_len)
+        assert (info["n_nodes"], info["n_tokens"], info["n_tiles"], info["n_paths"]) == \
+            (len(wl.parent), p["n_tokens"], p["n_tiles"], p["n_paths"])
+        assert info["max_nnz"] == p["n_tiles"] * (p["n_tiles"] + 1) // 2
+
+
+@pytest.mark.parametrize("parent,lens", [([0], [3]), ([-1, 5], [1, 1]), ([1, 0], [1, 1]), ([-1, 2, 1], [1, 1, 1]),
+                                         ([-1, 0], [1, -1]), ([-1, 0], [0, 0]), ([-1], [2 ** 31 - 1])])
+def test_plan_query_rejects(parent, lens):
+    if lens == [2 ** 31 - 1]:
+        info = tam.tree_plan_query(parent, lens)     # exactly at the limit: accepted
+        assert info["n_tokens"] == 2 ** 31 - 1
+        with pytest.raises(tam.TreeError):
+            tam.tree_plan_query([-1, 0], [2 ** 31 - 1, 1])
+        return
+    with pytest.raises(tam.TreeError) as e:
+        tam.tree_plan_query(parent, lens)
+    assert e.value.code == -1
+
+
+def test_plan_query_agrees_with_oracle_validation():
+    for s in range(40):
+        rng = np.random.default_rng(s)
+        n = int(rng.integers(1, 12))
+        parent = rng.integers(-1, n, size=n)
+        lens = rng.integers(-1, 4, size=n)
+        try:
+            oracle.validate_tree(parent, lens)
+            ok = True
+        except oracle.TreeError:
+            ok = False
+        try:
+            tam.tree_plan_query(parent, lens)
+            ok2 = True
+        except tam.TreeError:
+            ok2 = False
+        assert ok == ok2, (parent, lens)
+
+
+def test_strerror_and_version(lib):
+    lib.tree_strerror.restype = ctypes.c_char_p
+    for code in (0, -1, -2, -3, -4, -5, -6, 99):
+        assert lib.tree_strerror(code)
+    assert lib.tree_version() >= 1
+
+
+def test_bind_rejects_misaligned(lib):
+    wl = make_workload("tiny")
+    info = tam.PlanInfo()
+    par = np.asarray(wl.parent, np.int32)
+    nl = np.asarray(wl.node_len, np.int32)
+    assert tam._lib().tree_plan_query(par.ctypes.data, nl.ctypes.data, len(par), ctypes.byref(info)) == 0
+    c = tam.PlanT()
+    assert tam._lib().tree_plan_bind(ctypes.byref(info), ctypes.c_void_p(4096 + 8), ctypes.byref(c)) == -6
+    assert tam._lib().tree_plan_bind(ctypes.byref(info), ctypes.c_void_p(4096 * 16), ctypes.byref(c)) == 0
+    # carved pointers stay inside the buffer and are 256-byte aligned
+    for f in tam.PLAN_PTR_FIELDS:
+        off = getattr(c, f) - 4096 * 16
+        assert 0 <= off < info.plan_bytes and off % 4 == 0

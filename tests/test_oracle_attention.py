@@ -287,3 +287,21 @@ def test_nodes_formulation_matches_paths_caterpillar():
     b = oracle.attention_nodes(parent, node_len, q, k, v, u, p=plan, row_chunk=100)
     for key in ("o", "lse", "dq", "dk", "dv"):
         assert np.abs(a[key] - b[key]).max() < 1e-10, key
+
+
+def test_nodes_selection_exact_on_selected_leaf():
+    """Restricting the per-node form to some query nodes leaves their rows (O, LSE, dQ) and
+    the keys only they can see (a leaf's own dK, dV) exactly as in the full computation."""
+    parent, node_len = caterpillar_tree(p=20, T=6, delta=9, a=5)
+    N = int(node_len.sum())
+    q, k, v, u = _inputs(N, 2, 1, 16, seed=4)
+    plan = oracle.plan(parent, node_len)
+    full = oracle.attention_nodes(parent, node_len, q, k, v, u, p=plan)
+    leaves = [2, 12]
+    part = oracle.attention_nodes(parent, node_len, q, k, v, u, p=plan, nodes=leaves)
+    rows = np.concatenate([np.arange(plan["tok_start"][x], plan["tok_start"][x] + node_len[x]) for x in leaves])
+    for key in ("o", "dq"):
+        assert np.abs(full[key][rows] - part[key][rows]).max() < 1e-13
+    assert np.abs(full["lse"][:, rows] - part["lse"][:, rows]).max() < 1e-13
+    for key in ("dk", "dv"):
+        assert np.abs(full[key][rows] - part[key][rows]).max() < 1e-13

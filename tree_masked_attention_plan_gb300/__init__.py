@@ -1,0 +1,293 @@
+"""Python binding of the tree-masked attention library (GB300, sm_103a).
+
+Thin ctypes layer over ``_lib/libtreeattn.so``: it allocates outputs with PyTorch, passes
+``data_ptr()`` and the current CUDA stream, and turns status codes into exceptions.  Every
+step of the computation runs in the library's CUDA kernels; there is no fallback.  The
+functions carry the C entry points' names (``include/tree_attn.h``):
+
+  tree_plan_query, tree_plan, tree_rope_fwd, tree_apply_weights, tree_attn_fwd,
+  tree_attn_bwd_workspace, tree_attn_bwd, tree_selftest_timeout, tree_set_wait_limit_ns
+
+Semantics follow "Tree Training 技术详解" (tingdeliu.github.io): DFS packing (section 3.2),
+tree mask (4.2), block table (4.3), depth positions (5), path-count weights (6.2).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libtreeattn.so")
+TILE = 128
+
+TREE_OK = 0
+ERROR_NAMES = {-1: "TREE_ERR_INVALID_TREE", -2: "TREE_ERR_SHAPE", -3: "TREE_ERR_ARCH", -4: "TREE_ERR_CUDA",
+               -5: "TREE_ERR_TIMEOUT", -6: "TREE_ERR_ARG"}
+
+_i32, _i64, _vp, _f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_float
+
+
+class TreeError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = code
+        msg = f"{where}: {ERROR_NAMES.get(code, code)}"
+        try:
+            msg += f" ({_lib().tree_strerror(code).decode()})"
+            if code == -4:
+                msg += f": {_lib().tree_last_cuda_error().decode()}"
+        except Exception:  # pragma: no cover - message decoration only
+            pass
+        super().__init__(msg)
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("n_nodes", _i32), ("n_tokens", _i32), ("n_tiles", _i32), ("n_paths", _i32),
+                ("max_nnz", _i64), ("plan_bytes", _i64)]
+
+
+PLAN_PTR_FIELDS = ["order", "dfs_in", "dfs_out", "tok_start", "depth_off", "leaves", "dfs_tok_start", "sub_end",
+                   "tok_node", "pos", "g", "tok_in", "tok_out", "hi", "w", "tile_class", "row_ptr", "row_idx",
+                   "col_ptr", "col_idx", "row_order", "col_order", "tile_hi_min", "tile_hi_max", "counts"]
+
+
+class PlanT(ctypes.Structure):
+    _fields_ = [(f, _vp) for f in PLAN_PTR_FIELDS] + [("n_nodes", _i32), ("n_tokens", _i32),
+                                                      ("n_tiles", _i32), ("n_paths", _i32)]
+
+
+_LIB = None
+
+
+def _lib():
+    """Load the in-tree library; fails loudly when it has not been built."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with "
+                          "`python -m tree_masked_attention_plan_gb300.build_lib`")
+    lib = ctypes.CDLL(LIB_PATH)
+    P = ctypes.POINTER
+    sig = {
+        "tree_plan_query": (_i32, [_vp, _vp, _i32, P(PlanInfo)]),
+        "tree_plan_bind": (_i32, [P(PlanInfo), _vp, P(PlanT)]),
+        "tree_plan": (_i32, [_vp, _vp, _i32, P(PlanT), _vp]),
+        "tree_rope_fwd": (_i32, [P(PlanT), _vp, _vp, _vp, _vp, _i32, _i32, _i32, _f32, _vp]),
+        "tree_apply_weights": (_i32, [P(PlanT), _vp, _vp, _i32, _i32, _vp]),
+        "tree_attn_fwd": (_i32, [P(PlanT), _vp, _vp, _vp, _i32, _i32, _i32, _f32, _vp, _vp, _vp, _vp]),
+        "tree_attn_bwd_workspace": (ctypes.c_size_t, [P(PlanT), _i32, _i32]),
+        "tree_attn_bwd": (_i32, [P(PlanT), _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _f32, _f32, _vp,
+                                 _vp, _vp, _vp, _vp, _vp]),
+        "tree_set_wait_limit_ns": (_i32, [_i64]),
+        "tree_set_timing_events": (_i32, [ctypes.POINTER(_vp), _i32]),
+        "tree_selftest_timeout": (_i32, [_vp, _i64, _vp]),
+        "tree_strerror": (ctypes.c_char_p, [_i32]),
+        "tree_last_cuda_error": (ctypes.c_char_p, []),
+        "tree_version": (_i32, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _LIB = lib
+    return lib
+
+
+def _check(code, where):
+    if code != TREE_OK:
+        raise TreeError(code, where)
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _host_i32(a):
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def tree_plan_query(parent, node_len) -> dict:
+    """Validate a tree and return its sizes (host only)."""
+    par, nl = _host_i32(parent), _host_i32(node_len)
+    if par.shape != nl.shape:
+        raise ValueError("parent and node_len differ in length")
+    info = PlanInfo()
+    _check(_lib().tree_plan_query(par.ctypes.data, nl.ctypes.data, len(par), ctypes.byref(info)),
+           "tree_plan_query")
+    return {f: getattr(info, f) for f, _ in PlanInfo._fields_}
+
+
+@dataclass
+class TreePlan:
+    """A plan resident in device memory (one buffer) plus its C descriptor."""
+    info: PlanInfo
+    buf: torch.Tensor
+    c: PlanT
+    device: torch.device
+
+    @property
+    def n_tokens(self):
+        return self.info.n_tokens
+
+    @property
+    def n_tiles(self):
+        return self.info.n_tiles
+
+    @property
+    def n_pad(self):
+        return self.info.n_tiles * TILE
+
+    @property
+    def n_paths(self):
+        return self.info.n_paths
+
+    def ref(self):
+        return ctypes.byref(self.c)
+
+    def arrays(self) -> dict:
+        """Device tensor views of every plan array (for inspection and tests)."""
+        n, Np, T, nnz = self.info.n_nodes, self.n_pad, self.n_tiles, self.info.max_nnz
+        sizes = dict(order=n, dfs_in=n, dfs_out=n, tok_start=n, depth_off=n, leaves=n, dfs_tok_start=n,
+                     sub_end=n, tok_node=Np, pos=Np, g=Np, tok_in=Np, tok_out=Np, hi=Np, w=Np,
+                     tile_class=T * T, row_ptr=T + 1, row_idx=nnz, col_ptr=T + 1, col_idx=nnz, row_order=T,
+                     col_order=T, tile_hi_min=T, tile_hi_max=T, counts=4)
+        base = self.buf.data_ptr()
+        out = {}
+        for f in PLAN_PTR_FIELDS:
+            off = getattr(self.c, f) - base
+            if f == "tile_class":
+                out[f] = self.buf[off:off + sizes[f]]
+            else:
+                view = self.buf[off:off + 4 * sizes[f]]
+                out[f] = view.view(torch.float32 if f == "w" else torch.int32)
+        return out
+
+
+def tree_plan(parent, node_len, device=None, stream=None) -> TreePlan:
+    """Build the plan of a tree on the GPU (DFS order, intervals, positions, g, w, tile table)."""
+    par, nl = _host_i32(parent), _host_i32(node_len)
+    if par.shape != nl.shape:
+        raise ValueError("parent and node_len differ in length")
+    lib = _lib()
+    info = PlanInfo()
+    _check(lib.tree_plan_query(par.ctypes.data, nl.ctypes.data, len(par), ctypes.byref(info)), "tree_plan_query")
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    buf = torch.empty(int(info.plan_bytes), dtype=torch.uint8, device=dev)
+    c = PlanT()
+    _check(lib.tree_plan_bind(ctypes.byref(info), _ptr(buf), ctypes.byref(c)), "tree_plan_bind")
+    with torch.cuda.device(dev):
+        _check(lib.tree_plan(par.ctypes.data, nl.ctypes.data, len(par), ctypes.byref(c), _stream(stream)),
+               "tree_plan")
+    return TreePlan(info=info, buf=buf, c=c, device=dev)
+
+
+def _need(t, shape, dtype, name):
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous() or not t.is_cuda:
+        raise ValueError(f"{name}: expected contiguous CUDA {dtype} {tuple(shape)}, got {t.dtype} "
+                         f"{tuple(t.shape)} contiguous={t.is_contiguous()} cuda={t.is_cuda}")
+
+
+def _heads(plan, q, k):
+    N = plan.n_tokens
+    if q.dim() != 3 or k.dim() != 3:
+        raise ValueError("q, k must be [N, heads, d]")
+    Hq, d = q.shape[1], q.shape[2]
+    Hkv = k.shape[1]
+    _need(q, (N, Hq, d), torch.bfloat16, "q")
+    _need(k, (N, Hkv, d), torch.bfloat16, "k")
+    return Hq, Hkv, d
+
+
+def tree_rope_fwd(plan: TreePlan, q, k, theta=10000.0, qr=None, kr=None, stream=None):
+    """Rotate-half RoPE at depth positions: returns (qr, kr); pass qr=q, kr=k for in place."""
+    Hq, Hkv, d = _heads(plan, q, k)
+    qr = torch.empty_like(q) if qr is None else qr
+    kr = torch.empty_like(k) if kr is None else kr
+    _check(_lib().tree_rope_fwd(plan.ref(), _ptr(q), _ptr(k), _ptr(qr), _ptr(kr), Hq, Hkv, d, float(theta),
+                                _stream(stream)), "tree_rope_fwd")
+    return qr, kr
+
+
+def tree_apply_weights(plan: TreePlan, u, out=None, stream=None):
+    """dO = (g_t / K) * U_t for u [N, H, d] bf16."""
+    N, H, d = u.shape
+    _need(u, (plan.n_tokens, H, d), torch.bfloat16, "u")
+    out = torch.empty_like(u) if out is None else out
+    _check(_lib().tree_apply_weights(plan.ref(), _ptr(u), _ptr(out), H, d, _stream(stream)), "tree_apply_weights")
+    return out
+
+
+def tree_attn_fwd(plan: TreePlan, q, k, v, scale=0.0, o=None, lse=None, status=None, stream=None):
+    """Tree-masked attention forward: returns (o [N,Hq,d] bf16, lse [Hq, N_pad] fp32)."""
+    Hq, Hkv, d = _heads(plan, q, k)
+    _need(v, k.shape, torch.bfloat16, "v")
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty(Hq, plan.n_pad, dtype=torch.float32, device=q.device) if lse is None else lse
+    _need(lse, (Hq, plan.n_pad), torch.float32, "lse")
+    _check(_lib().tree_attn_fwd(plan.ref(), _ptr(q), _ptr(k), _ptr(v), Hq, Hkv, d, float(scale), _ptr(o), _ptr(lse),
+                                _ptr(status), _stream(stream)), "tree_attn_fwd")
+    return o, lse
+
+
+def tree_attn_bwd_workspace(plan: TreePlan, Hq: int, d: int) -> int:
+    return int(_lib().tree_attn_bwd_workspace(plan.ref(), Hq, d))
+
+
+def tree_attn_bwd(plan: TreePlan, q, k, v, o, lse, dO, scale=0.0, rope_theta=10000.0, workspace=None,
+                  dq=None, dk=None, dv=None, status=None, stream=None):
+    """Backward: returns (dq, dk, dv); with rope_theta > 0 dq/dk are w.r.t. the un-rotated q, k."""
+    Hq, Hkv, d = _heads(plan, q, k)
+    _need(v, k.shape, torch.bfloat16, "v")
+    _need(o, q.shape, torch.bfloat16, "o")
+    _need(dO, q.shape, torch.bfloat16, "dO")
+    _need(lse, (Hq, plan.n_pad), torch.float32, "lse")
+    if workspace is None:
+        workspace = torch.empty(tree_attn_bwd_workspace(plan, Hq, d), dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check(_lib().tree_attn_bwd(plan.ref(), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), Hq, Hkv, d,
+                                float(scale), float(rope_theta), _ptr(workspace), _ptr(dq), _ptr(dk), _ptr(dv),
+                                _ptr(status), _stream(stream)), "tree_attn_bwd")
+    return dq, dk, dv
+
+
+def tree_set_timing_events(events):
+    """Register torch.cuda.Event objects (up to 4, enable_timing=True) that tree_attn_bwd records
+    around its kernels: before delta, before dK/dV, after dK/dV, after dQ finalize.  [] clears."""
+    arr = (_vp * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    _check(_lib().tree_set_timing_events(arr, len(events)), "tree_set_timing_events")
+
+
+def tree_set_wait_limit_ns(ns: int):
+    _check(_lib().tree_set_wait_limit_ns(int(ns)), "tree_set_wait_limit_ns")
+
+
+def tree_selftest_timeout(status, ns: int = 1_000_000, stream=None):
+    _check(_lib().tree_selftest_timeout(_ptr(status), int(ns), _stream(stream)), "tree_selftest_timeout")
+
+
+def new_status(device=None):
+    """A zeroed int32 device status word for the kernels' error reports."""
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def check_status(status, where="device"):
+    """Raise TreeError if a kernel stored an error code in `status` (synchronizes)."""
+    code = int(status.item())
+    if code != TREE_OK:
+        raise TreeError(code, where)
+
+
+__all__ = ["TreeError", "TreePlan", "tree_plan_query", "tree_plan", "tree_rope_fwd", "tree_apply_weights",
+           "tree_attn_fwd", "tree_attn_bwd_workspace", "tree_attn_bwd", "tree_set_wait_limit_ns",
+           "tree_selftest_timeout", "tree_set_timing_events", "new_status", "check_status", "LIB_PATH", "TILE"]

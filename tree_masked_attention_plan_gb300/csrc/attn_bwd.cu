@@ -1,0 +1,492 @@
+// Tree-masked attention backward on tcgen05 ("Tree Training 技术详解", section 6.2 and
+// section 7: a shared ancestor's K/V receive the summed gradients of every descendant that
+// sees them).  Three kernels:
+//   k_bwd_pre      delta_i = sum_c dO_ic O_ic per (token, q head); zero the fp32 dQ accumulator.
+//   k_bwd_dkdv     one CTA per (key tile, kv head): loops over the q heads of the group and the
+//                  non-empty query tiles of the key tile's column.  Per step, in TMEM:
+//                    S^T  = K Q^T            (cols   0..127, lane = key)
+//                    dP^T = V dO^T           (cols 128..255)
+//                  the elementwise warps form P^T = exp2(S^T scale log2e - LSE log2e) (masked on
+//                  partial tiles) and dS^T = P^T (dP^T - delta) scale as bf16 in shared memory;
+//                    dV  += P^T dO           (cols 256..256+d)     accumulated on chip,
+//                    dK  += dS^T Q           (cols 256+d..256+2d)  written once at the end,
+//                    dQ   = dS K             (cols   0..d, lane = query), added to the fp32
+//                                            accumulator with coalesced red.global.add.
+//                  dK gets the inverse RoPE rotation in the epilogue.
+//   k_dq_finalize  dQ = R(pos)^T dQacc, fp32 -> bf16, token-major.
+#include <algorithm>
+#include <cmath>
+
+#include "common.cuh"
+
+namespace ta {
+namespace {
+
+constexpr int kBwdThreads = 192;
+
+template <int HD>
+struct BwdCfg {
+  static constexpr int NCH = HD / 64;
+  static constexpr int K_OFF = 0;
+  static constexpr int V_OFF = K_OFF + NCH * CHUNK_BYTES;
+  static constexpr int Q_OFF = V_OFF + NCH * CHUNK_BYTES;
+  static constexpr int DO_OFF = Q_OFF + NCH * CHUNK_BYTES;
+  static constexpr int PT_OFF = DO_OFF + NCH * CHUNK_BYTES;
+  static constexpr int DST_OFF = PT_OFF + 2 * CHUNK_BYTES;
+  static constexpr int LSE_OFF = DST_OFF + 2 * CHUNK_BYTES;
+  static constexpr int DLT_OFF = LSE_OFF + TILE * 4;
+  static constexpr int QIN_OFF = DLT_OFF + TILE * 4;
+  static constexpr int BAR_OFF = QIN_OFF + TILE * 4;
+  static constexpr int NBAR = 9;
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int SMEM = MISC_OFF + 16;
+  static constexpr int SMEM_ALLOC = SMEM + 1024;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t ST_COL = 0, DPT_COL = 128, DV_COL = 256, DK_COL = 256 + HD, DQ_COL = 0;
+  static constexpr uint32_t IDESC_SDP = idesc_bf16(TILE, TILE, 0, 0);   // K/V K-major, Q/dO K-major
+  static constexpr uint32_t IDESC_DKV = idesc_bf16(TILE, HD, 0, 1);     // P^T/dS^T K-major, dO/Q MN-major
+  static constexpr uint32_t IDESC_DQ = idesc_bf16(TILE, HD, 1, 1);      // dS MN-major, K MN-major
+  static constexpr uint32_t KV_TX = 2 * NCH * CHUNK_BYTES;
+  static constexpr uint32_t QDO_TX = 2 * NCH * CHUNK_BYTES + 3 * TILE * 4;
+};
+
+struct BwdParams {
+  const int32_t* col_ptr;
+  const int32_t* col_idx;
+  const int32_t* col_order;
+  const int32_t* tok_in;
+  const int32_t* tok_out;
+  const int32_t* pos;
+  const uint8_t* tile_class;
+  const float* lse;          // [Hq][Npad]
+  const float* dlt;          // [Hq][Npad]
+  float* dqacc;              // [Hq][HD][Npad]
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int32_t* status;
+  int N, T, Npad, Hq, Hkv, grp;
+  float scale, scale_log2, rope_theta;
+  uint64_t wait_ns;
+};
+
+DEVI uint8_t* align1024b(uint8_t* p) {
+  const uint32_t a = smem_u32(p);
+  return p + ((1024u - (a & 1023u)) & 1023u);
+}
+
+DEVI void mbar_wait_drain_b(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > limit_ns) return;
+}
+
+// ------------------------------------------------------------------------------------------
+// delta and accumulator zeroing: one group of HD/8 threads per (token, q head) row
+template <int HD>
+__global__ void k_bwd_pre(const uint4* __restrict__ o, const uint4* __restrict__ dO, float* dlt, int N, int Npad,
+                          int Hq) {
+  constexpr int TPR = HD / 8;
+  const size_t gt = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t row = gt / TPR;                  // row = token * Hq + h
+  const int sub = static_cast<int>(gt % TPR);
+  const size_t rows = (size_t)Npad * Hq;
+  float acc = 0.f;
+  const int tok = static_cast<int>(row / Hq);
+  if (row < rows && tok < N) {
+    const uint4 a = o[row * TPR + sub], b = dO[row * TPR + sub];
+    acc = bf16lo(a.x) * bf16lo(b.x) + bf16hi(a.x) * bf16hi(b.x) + bf16lo(a.y) * bf16lo(b.y) +
+          bf16hi(a.y) * bf16hi(b.y) + bf16lo(a.z) * bf16lo(b.z) + bf16hi(a.z) * bf16hi(b.z) +
+          bf16lo(a.w) * bf16lo(b.w) + bf16hi(a.w) * bf16hi(b.w);
+  }
+#pragma unroll
+  for (int off = TPR / 2; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (row < rows && sub == 0) {
+    const int h = static_cast<int>(row % Hq);
+    dlt[(size_t)h * Npad + tok] = acc;
+  }
+}
+
+__global__ void k_zero_f32x4(float4* p, size_t n4) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x)
+    p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// ------------------------------------------------------------------------------------------
+template <int HD>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    k_bwd_dkdv(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+               const BwdParams p) {
+  using C = BwdCfg<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024b(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::BAR_OFF);
+  uint64_t* kv_full = bars + 0;
+  uint64_t* qdo_full = bars + 1;
+  uint64_t* qdo_empty = bars + 2;
+  uint64_t* sdp_full = bars + 3;
+  uint64_t* ds_ready = bars + 4;
+  uint64_t* dq_full = bars + 5;
+  uint64_t* dq_free = bars + 6;
+  uint64_t* dkdv_done = bars + 7;
+  uint64_t* drain = bars + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::MISC_OFF);
+  int* abort_flag = reinterpret_cast<int*>(sm + C::MISC_OFF + 4);
+  float* lse_s = reinterpret_cast<float*>(sm + C::LSE_OFF);
+  float* dlt_s = reinterpret_cast<float*>(sm + C::DLT_OFF);
+  int32_t* qin_s = reinterpret_cast<int32_t*>(sm + C::QIN_OFF);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int u = blockIdx.x;
+  const int kt = p.col_order[u / p.Hkv];
+  const int kvh = u % p.Hkv;
+  const int cp0 = p.col_ptr[kt];
+  const int ccnt = p.col_ptr[kt + 1] - cp0;
+  const int total = ccnt * p.grp;               // steps: q head (outer) x query tile (inner)
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    mbar_init(qdo_full, 1);
+    mbar_init(qdo_empty, 1);
+    mbar_init(sdp_full, 1);
+    mbar_init(ds_ready, 128);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_free, 128);
+    mbar_init(dkdv_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl wc{abort_flag, p.status, p.wait_ns};
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      prefetch_tmap(&tmDO);
+      mbar_expect_tx(kv_full, C::KV_TX);
+      for (int c = 0; c < C::NCH; ++c) {
+        tma_load_3d(sm + C::K_OFF + c * CHUNK_BYTES, &tmK, kv_full, c * 64, kvh, kt * TILE);
+        tma_load_3d(sm + C::V_OFF + c * CHUNK_BYTES, &tmV, kv_full, c * 64, kvh, kt * TILE);
+      }
+      int issued = 0;
+      for (int n = 0; n < total; ++n) {
+        const int h = kvh * p.grp + n / ccnt;
+        const int qt = p.col_idx[cp0 + n % ccnt];
+        if (n > 0 && !mbar_wait(qdo_empty, (n - 1) & 1, wc)) break;
+        mbar_expect_tx(qdo_full, C::QDO_TX);
+        for (int c = 0; c < C::NCH; ++c) {
+          tma_load_3d(sm + C::Q_OFF + c * CHUNK_BYTES, &tmQ, qdo_full, c * 64, h, qt * TILE);
+          tma_load_3d(sm + C::DO_OFF + c * CHUNK_BYTES, &tmDO, qdo_full, c * 64, h, qt * TILE);
+        }
+        const size_t lo = (size_t)h * p.Npad + (size_t)qt * TILE;
+        bulk_load(lse_s, p.lse + lo, TILE * 4, qdo_full);
+        bulk_load(dlt_s, p.dlt + lo, TILE * 4, qdo_full);
+        bulk_load(qin_s, p.tok_in + (size_t)qt * TILE, TILE * 4, qdo_full);
+        issued = n + 1;
+      }
+      if (*abort_flag) {
+        mbar_wait_drain_b(kv_full, 0, p.wait_ns);
+        if (issued > 0) mbar_wait_drain_b(qdo_full, (issued - 1) & 1, p.wait_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t k_base = smem_u32(sm + C::K_OFF), v_base = smem_u32(sm + C::V_OFF);
+      const uint32_t q_base = smem_u32(sm + C::Q_OFF), do_base = smem_u32(sm + C::DO_OFF);
+      const uint32_t pt_base = smem_u32(sm + C::PT_OFF), dst_base = smem_u32(sm + C::DST_OFF);
+      bool ok = mbar_wait(kv_full, 0, wc);
+      for (int n = 0; ok && n < total; ++n) {
+        if (!mbar_wait(qdo_full, n & 1, wc)) { ok = false; break; }
+        if (n > 0 && !mbar_wait(dq_free, (n - 1) & 1, wc)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {                 // S^T = K Q^T, dP^T = V dO^T
+          const uint32_t off = (kk >> 2) * CHUNK_BYTES + (kk & 3) * 32;
+          umma_bf16(tmem + C::ST_COL, sdesc_sw128(k_base + off, 16, 1024), sdesc_sw128(q_base + off, 16, 1024),
+                    C::IDESC_SDP, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * CHUNK_BYTES + (kk & 3) * 32;
+          umma_bf16(tmem + C::DPT_COL, sdesc_sw128(v_base + off, 16, 1024), sdesc_sw128(do_base + off, 16, 1024),
+                    C::IDESC_SDP, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(sdp_full);
+        if (!mbar_wait(ds_ready, n & 1, wc)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < TILE / 16; ++kk) {               // dV += P^T dO, dK += dS^T Q
+          const uint32_t a_off = (kk >> 2) * CHUNK_BYTES + (kk & 3) * 32;
+          const uint32_t b_off = kk * 16 * 128;
+          const uint32_t acc = (n > 0 || kk > 0) ? 1u : 0u;
+          umma_bf16(tmem + C::DV_COL, sdesc_sw128(pt_base + a_off, 16, 1024),
+                    sdesc_sw128(do_base + b_off, CHUNK_BYTES, 1024), C::IDESC_DKV, acc);
+          umma_bf16(tmem + C::DK_COL, sdesc_sw128(dst_base + a_off, 16, 1024),
+                    sdesc_sw128(q_base + b_off, CHUNK_BYTES, 1024), C::IDESC_DKV, acc);
+        }
+#pragma unroll
+        for (int kk = 0; kk < TILE / 16; ++kk) {               // dQ = dS K  (keys along K)
+          const uint32_t off = kk * 16 * 128;
+          umma_bf16(tmem + C::DQ_COL, sdesc_sw128(dst_base + off, CHUNK_BYTES, 1024),
+                    sdesc_sw128(k_base + off, CHUNK_BYTES, 1024), C::IDESC_DQ, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(dq_full);
+        umma_commit(qdo_empty);
+      }
+      if (ok) umma_commit(dkdv_done);
+      umma_commit(drain);
+      mbar_wait_drain_b(drain, 0, p.wait_ns);
+    }
+  } else {
+    // ---------------------------------------------------------------- elementwise warps
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;                 // key row for S^T/dP^T/dK/dV, query row for dQ
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const int j = kt * TILE + r;
+    const int kin = p.tok_in[j], kout = p.tok_out[j];
+    const float nl2e = -1.4426950408889634f;
+    bool ok = true;
+    for (int n = 0; n < total; ++n) {
+      const int h = kvh * p.grp + n / ccnt;
+      const int qt = p.col_idx[cp0 + n % ccnt];
+      const uint8_t cls = p.tile_class[(size_t)qt * p.T + kt];
+      if (!mbar_wait(qdo_full, n & 1, wc) || !mbar_wait(sdp_full, n & 1, wc)) { ok = false; break; }
+      tc_fence_after();
+      const int jrel = j - qt * TILE;             // query i is causal-visible iff i >= jrel
+#pragma unroll 1
+      for (int jc = 0; jc < TILE / 32; ++jc) {
+        uint32_t sr[32], dr[32];
+        tmem_ld32(lane_base + C::ST_COL + jc * 32, sr);
+        tmem_ld32(lane_base + C::DPT_COL + jc * 32, dr);
+        tmem_wait_ld(sr);
+        tmem_wait_ld(dr);
+        uint32_t pp[16], dd[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float pv[2], dv_[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int i = jc * 32 + c + e;
+            float pe = ex2_approx(fmaf(__uint_as_float(sr[c + e]), p.scale_log2, lse_s[i] * nl2e));
+            if (cls == 1) {
+              const int qi_in = qin_s[i];
+              const bool vis = (i >= jrel) && (kin <= qi_in) && (qi_in <= kout);
+              pe = vis ? pe : 0.f;
+            }
+            pv[e] = pe;
+            dv_[e] = pe * (__uint_as_float(dr[c + e]) - dlt_s[i]) * p.scale;
+          }
+          pp[c >> 1] = pack_bf16(pv[0], pv[1]);
+          dd[c >> 1] = pack_bf16(dv_[0], dv_[1]);
+        }
+        uint8_t* ptb = sm + C::PT_OFF + (jc >> 1) * CHUNK_BYTES;
+        uint8_t* dsb = sm + C::DST_OFF + (jc >> 1) * CHUNK_BYTES;
+#pragma unroll
+        for (int uu = 0; uu < 4; ++uu) {
+          const int unit = (jc & 1) * 4 + uu;
+          st_swizzled_unit(ptb, r, unit, make_uint4(pp[4 * uu], pp[4 * uu + 1], pp[4 * uu + 2], pp[4 * uu + 3]));
+          st_swizzled_unit(dsb, r, unit, make_uint4(dd[4 * uu], dd[4 * uu + 1], dd[4 * uu + 2], dd[4 * uu + 3]));
+        }
+      }
+      tc_fence_before();
+      fence_proxy_async_smem();
+      mbar_arrive(ds_ready);
+      if (!mbar_wait(dq_full, n & 1, wc)) { ok = false; break; }
+      tc_fence_after();
+      const int qi = qt * TILE + r;
+      float* dst = p.dqacc + (size_t)h * HD * p.Npad + qi;
+#pragma unroll 1
+      for (int jc = 0; jc < HD / 32; ++jc) {
+        uint32_t qr[32];
+        tmem_load32(lane_base + C::DQ_COL + jc * 32, qr);
+        if (qi < p.N) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) atomicAdd(dst + (size_t)(jc * 32 + c) * p.Npad, __uint_as_float(qr[c]));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(dq_free);
+    }
+    if (ok && mbar_wait(dkdv_done, 0, wc)) {
+      tc_fence_after();
+      // dV row j
+      __nv_bfloat16* dvrow = p.dv + ((size_t)j * p.Hkv + kvh) * HD;
+#pragma unroll 1
+      for (int jc = 0; jc < HD / 32; ++jc) {
+        uint32_t a[32];
+        tmem_load32(lane_base + C::DV_COL + jc * 32, a);
+        if (j < p.N) {
+          uint4* d4 = reinterpret_cast<uint4*>(dvrow + jc * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            d4[v] = make_uint4(pack_bf16(__uint_as_float(a[8 * v + 0]), __uint_as_float(a[8 * v + 1])),
+                               pack_bf16(__uint_as_float(a[8 * v + 2]), __uint_as_float(a[8 * v + 3])),
+                               pack_bf16(__uint_as_float(a[8 * v + 4]), __uint_as_float(a[8 * v + 5])),
+                               pack_bf16(__uint_as_float(a[8 * v + 6]), __uint_as_float(a[8 * v + 7])));
+        }
+      }
+      // dK row j with the inverse RoPE rotation: columns c and c + HD/2 pair up
+      __nv_bfloat16* dkrow = p.dk + ((size_t)j * p.Hkv + kvh) * HD;
+      const float posf = (j < p.N) ? static_cast<float>(p.pos[j]) : 0.f;
+#pragma unroll 1
+      for (int jc = 0; jc < HD / 64; ++jc) {
+        uint32_t a[32], b[32];
+        tmem_load32(lane_base + C::DK_COL + jc * 32, a);
+        tmem_load32(lane_base + C::DK_COL + HD / 2 + jc * 32, b);
+        float lo[32], hi[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float g1 = __uint_as_float(a[c]), g2 = __uint_as_float(b[c]);
+          if (p.rope_theta > 0.f) {
+            float sv, cv;
+            sincosf(posf * rope_inv_freq(jc * 32 + c, HD, p.rope_theta), &sv, &cv);
+            lo[c] = g1 * cv + g2 * sv;
+            hi[c] = g2 * cv - g1 * sv;
+          } else {
+            lo[c] = g1;
+            hi[c] = g2;
+          }
+        }
+        if (j < p.N) {
+          uint4* d4 = reinterpret_cast<uint4*>(dkrow + jc * 32);
+          uint4* e4 = reinterpret_cast<uint4*>(dkrow + HD / 2 + jc * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            d4[v] = make_uint4(pack_bf16(lo[8 * v], lo[8 * v + 1]), pack_bf16(lo[8 * v + 2], lo[8 * v + 3]),
+                               pack_bf16(lo[8 * v + 4], lo[8 * v + 5]), pack_bf16(lo[8 * v + 6], lo[8 * v + 7]));
+            e4[v] = make_uint4(pack_bf16(hi[8 * v], hi[8 * v + 1]), pack_bf16(hi[8 * v + 2], hi[8 * v + 3]),
+                               pack_bf16(hi[8 * v + 4], hi[8 * v + 5]), pack_bf16(hi[8 * v + 6], hi[8 * v + 7]));
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// dQ = R(pos)^T dQacc: one block per 32 tokens, all heads; angles computed once per token.
+template <int HD>
+__global__ void __launch_bounds__(256) k_dq_finalize(const float* __restrict__ dqacc, const int32_t* __restrict__ pos,
+                                                     __nv_bfloat16* dq, int N, int Npad, int Hq, float theta) {
+  constexpr int TT = 32, HALF = HD / 2;
+  __shared__ float s_cos[TT][HALF], s_sin[TT][HALF];
+  __shared__ float tile[HD][TT + 1];
+  const int i0 = blockIdx.x * TT;
+  for (int e = threadIdx.x; e < TT * HALF; e += blockDim.x) {
+    const int t = e / HALF, c = e % HALF;
+    const int i = i0 + t;
+    float sv = 0.f, cv = 1.f;
+    if (theta > 0.f && i < N) sincosf(static_cast<float>(pos[i]) * rope_inv_freq(c, HD, theta), &sv, &cv);
+    s_cos[t][c] = cv;
+    s_sin[t][c] = sv;
+  }
+  for (int h = 0; h < Hq; ++h) {
+    __syncthreads();
+    const float* src = dqacc + (size_t)h * HD * Npad + i0;
+    for (int e = threadIdx.x; e < HD * TT; e += blockDim.x) {
+      const int c = e / TT, t = e % TT;
+      tile[c][t] = src[(size_t)c * Npad + t];
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < TT * HALF; e += blockDim.x) {
+      const int t = e / HALF, c = e % HALF;
+      const int i = i0 + t;
+      if (i >= N) continue;
+      const float g1 = tile[c][t], g2 = tile[c + HALF][t];
+      const float cv = s_cos[t][c], sv = s_sin[t][c];
+      __nv_bfloat16* row = dq + ((size_t)i * Hq + h) * HD;
+      row[c] = __float2bfloat16_rn(g1 * cv + g2 * sv);
+      row[c + HALF] = __float2bfloat16_rn(g2 * cv - g1 * sv);
+    }
+  }
+}
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+template <int HD>
+int launch_bwd(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k, const tree_bf16* v,
+               const tree_bf16* o, const float* lse, const tree_bf16* dO, int Hq, int Hkv, float scale, float theta,
+               void* ws, tree_bf16* dq, tree_bf16* dk, tree_bf16* dv, int32_t* status, cudaStream_t s) {
+  using C = BwdCfg<HD>;
+  const int N = plan->n_tokens, T = plan->n_tiles, Npad = T * TILE;
+  float* dlt = static_cast<float*>(ws);
+  float* dqacc = reinterpret_cast<float*>(static_cast<char*>(ws) + align256((size_t)Hq * Npad * 4));
+  CUtensorMap tq, tk, tv, tdo;
+  int rc = make_tmap_bf16_3d(&tq, q, HD, Hq, N);
+  if (!rc) rc = make_tmap_bf16_3d(&tk, k, HD, Hkv, N);
+  if (!rc) rc = make_tmap_bf16_3d(&tv, v, HD, Hkv, N);
+  if (!rc) rc = make_tmap_bf16_3d(&tdo, dO, HD, Hq, N);
+  if (rc) return rc;
+  rc = record_cuda(cudaFuncSetAttribute(k_bwd_dkdv<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC));
+  if (rc) return rc;
+  record_timing_event(0, s);
+  {
+    const size_t threads = (size_t)Npad * Hq * (HD / 8);
+    k_bwd_pre<HD><<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(
+        reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dO), dlt, N, Npad, Hq);
+    const size_t n4 = (size_t)Hq * HD * Npad / 4;
+    k_zero_f32x4<<<(unsigned)std::min<size_t>((n4 + 255) / 256, 152 * 16), 256, 0, s>>>(
+        reinterpret_cast<float4*>(dqacc), n4);
+  }
+  BwdParams P{plan->col_ptr, plan->col_idx, plan->col_order, plan->tok_in, plan->tok_out, plan->pos,
+              plan->tile_class, lse, dlt, dqacc, reinterpret_cast<__nv_bfloat16*>(dk),
+              reinterpret_cast<__nv_bfloat16*>(dv), status, N, T, Npad, Hq, Hkv, Hq / Hkv, scale,
+              scale * 1.4426950408889634f, theta, wait_limit_ns()};
+  record_timing_event(1, s);
+  k_bwd_dkdv<HD><<<T * Hkv, kBwdThreads, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, P);
+  record_timing_event(2, s);
+  k_dq_finalize<HD><<<(N + 31) / 32, 256, 0, s>>>(dqacc, plan->pos, reinterpret_cast<__nv_bfloat16*>(dq), N, Npad,
+                                                  Hq, theta);
+  record_timing_event(3, s);
+  return record_cuda(cudaGetLastError());
+}
+
+}  // namespace
+}  // namespace ta
+
+using namespace ta;
+
+extern "C" size_t tree_attn_bwd_workspace(const tree_plan_t* plan, int Hq, int d) {
+  if (!plan || Hq <= 0 || d <= 0) return 0;
+  const size_t Np = (size_t)plan->n_tiles * TILE;
+  return align256(Np * Hq * 4) + align256((size_t)Hq * d * Np * 4);
+}
+
+extern "C" int tree_attn_bwd(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k, const tree_bf16* v,
+                             const tree_bf16* o, const float* lse, const tree_bf16* dO, int Hq, int Hkv, int d,
+                             float scale, float rope_theta, void* workspace, tree_bf16* dq, tree_bf16* dk,
+                             tree_bf16* dv, int32_t* status_dev, tree_stream_t stream) {
+  int rc = plan_ok(plan);
+  if (rc) return rc;
+  if (!q || !k || !v || !o || !lse || !dO || !workspace || !dq || !dk || !dv) return TREE_ERR_ARG;
+  if ((d != 64 && d != 128) || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return TREE_ERR_SHAPE;
+  for (const void* ptr : {(const void*)o, (const void*)dO, (const void*)dq, (const void*)dk, (const void*)dv})
+    if (reinterpret_cast<uintptr_t>(ptr) & 15) return TREE_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) || (reinterpret_cast<uintptr_t>(lse) & 15)) return TREE_ERR_ARG;
+  rc = check_device();
+  if (rc) return rc;
+  if (!(scale > 0.f)) scale = 1.f / sqrtf(static_cast<float>(d));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return d == 128 ? launch_bwd<128>(plan, q, k, v, o, lse, dO, Hq, Hkv, scale, rope_theta, workspace, dq, dk, dv,
+                                    status_dev, s)
+                  : launch_bwd<64>(plan, q, k, v, o, lse, dO, Hq, Hkv, scale, rope_theta, workspace, dq, dk, dv,
+                                   status_dev, s);
+}
