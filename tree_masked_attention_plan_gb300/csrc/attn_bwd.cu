@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int h = kvh * p.grp + n / ccnt;
       const int qt = p.col_idx[cp0 + n % ccnt];
       const uint8_t cls = p.tile_class[(size_t)qt * p.T + kt];
-      if (!mbar_wait(qdo_full, n & 1, wc) || !mbar_wait(sdp_full, n & 1, wc)) { ok = false; break; }
+      if (!mbar_wait_warp(qdo_full, n & 1, wc) || !mbar_wait_warp(sdp_full, n & 1, wc)) { ok = false; break; }
       tc_fence_after();
       const int jrel = j - qt * TILE;             // query i is causal-visible iff i >= jrel
 #pragma unroll 1
@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_before();
       fence_proxy_async_smem();
       mbar_arrive(ds_ready);
-      if (!mbar_wait(dq_full, n & 1, wc)) { ok = false; break; }
+      if (!mbar_wait_warp(dq_full, n & 1, wc)) { ok = false; break; }
       tc_fence_after();
       const int qi = qt * TILE + r;
       float* dst = p.dqacc + (size_t)h * HD * p.Npad + qi;
@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_before();
       mbar_arrive(dq_free);
     }
-    if (ok && mbar_wait(dkdv_done, 0, wc)) {
+    if (ok && mbar_wait_warp(dkdv_done, 0, wc)) {
       tc_fence_after();
       // dV row j
       __nv_bfloat16* dvrow = p.dv + ((size_t)j * p.Hkv + kvh) * HD;
@@ -376,6 +376,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }

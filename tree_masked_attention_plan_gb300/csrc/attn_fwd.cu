@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int b = n & 1, s = n % C::NS;
       const int kt = p.row_idx[rp0 + n];
       const uint8_t cls = p.tile_class[(size_t)qt * p.T + kt];
-      if (!mbar_wait(&s_full[b], (n >> 1) & 1, wc)) { ok = false; break; }
+      if (!mbar_wait_warp(&s_full[b], (n >> 1) & 1, wc)) { ok = false; break; }
       tc_fence_after();
       float sv[TILE];
 #pragma unroll
@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tc_fence_before();
       mbar_arrive(&s_free[b]);
       if (cls == 1) {                          // partial tile: tree mask in registers
-        if (!mbar_wait(&kv_full[s], (n / C::NS) & 1, wc)) { ok = false; break; }
+        if (!mbar_wait_warp(&kv_full[s], (n / C::NS) & 1, wc)) { ok = false; break; }
         const int4* kin4 = reinterpret_cast<const int4*>(kin_s + s * TILE);
         const int4* kout4 = reinterpret_cast<const int4*>(kout_s + s * TILE);
         const int jrel = qi - kt * TILE;       // key c is causal-visible iff c <= jrel
@@ -256,9 +256,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       l_run = l_run * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
       if (n > 0) {
-        if (!mbar_wait(pv_done, (n - 1) & 1, wc)) { ok = false; break; }
+        if (!mbar_wait_warp(pv_done, (n - 1) & 1, wc)) { ok = false; break; }
         tc_fence_after();
-        if (alpha != 1.f) {                    // rescale the TMEM accumulator row
+        // TMEM ld/st are warp-collective: rescale when any row of the warp needs it
+        // (rows whose max did not move have alpha == 1 and are multiplied exactly by 1)
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
           for (int j = 0; j < HD / 32; ++j) {
             uint32_t rr[32];
@@ -281,7 +283,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       m_run = m_new;
       m_ref = m_use;
     }
-    if (ok && cnt > 0 && mbar_wait(pv_done, (cnt - 1) & 1, wc)) {
+    if (ok && cnt > 0 && mbar_wait_warp(pv_done, (cnt - 1) & 1, wc)) {
       tc_fence_after();
       const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
       __nv_bfloat16* orow = p.o + ((size_t)qi * p.Hq + h) * HD;
@@ -309,6 +311,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }

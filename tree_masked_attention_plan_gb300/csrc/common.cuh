@@ -90,6 +90,14 @@ DEVI bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtl& wc) {
   }
 }
 
+// Warp-collective form for warps that go on to tcgen05.ld/st (.sync.aligned: every lane must
+// execute them together).  All lanes wait, then agree: if any lane gave up, all do, and the
+// warp leaves convergent either way.
+DEVI bool mbar_wait_warp(uint64_t* bar, uint32_t parity, const WaitCtl& wc) {
+  const bool ok = mbar_wait(bar, parity, wc);
+  return __all_sync(0xffffffffu, ok) != 0;
+}
+
 // ------------------------------------------------------------------------------------------
 // TMA
 DEVI void prefetch_tmap(const CUtensorMap* m) {
