@@ -264,6 +264,9 @@ def tree_attn_bwd(plan: TreePlan, q, k, v, o, lse, dO, scale=0.0, rope_theta=100
 def tree_set_timing_events(events):
     """Register torch.cuda.Event objects (up to 4, enable_timing=True) that tree_attn_bwd records
     around its kernels: before delta, before dK/dV, after dK/dV, after dQ finalize.  [] clears."""
+    for e in events:                       # torch creates the CUDA event on first record
+        if not e.cuda_event:
+            e.record()
     arr = (_vp * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
     _check(_lib().tree_set_timing_events(arr, len(events)), "tree_set_timing_events")
 

@@ -2,19 +2,22 @@
 // Softmax(Q K^T / sqrt(d) + M) V with the tree mask M; section 4.3: block-sparse over the
 // ancestor tiles, mask evaluated only where a tile is partly visible).
 //
-// One CTA computes one (query tile, q head) pair over the non-empty key tiles of its row:
-//   warp 0      TMA producer: Q tile once, then K/V tiles (plus their dfs_in/dfs_out words)
-//               into a 2-stage ring;
-//   warp 1      allocates TMEM and issues every tcgen05.mma from one thread:
-//               S_b = Q K^T into one of two TMEM score buffers, O += P V into the TMEM
-//               output accumulator;
-//   warps 2..5  softmax: thread r owns query row r (TMEM lane r), so the running max and
-//               sum of a row stay in that thread; partial tiles apply the interval mask
-//               dfs_in(node j) <= dfs_in(node i) <= dfs_out(node j) and j <= i; P goes to
-//               shared memory as bf16 in the 128-byte-swizzled K-major layout the MMA reads;
-//               O is rescaled in TMEM when the row max grows.
-// Online-softmax state per row is (m, l) in log2 units; two partial states combine with
-// the associative merge of the Tree Attention page (max of maxima, rescaled sums).
+// One CTA computes one query tile for NH q heads that read the same kv head (NH = 2 when the
+// GQA group size is even, else 1), walking the non-empty key tiles of the tile's row.  Each
+// K/V tile is loaded once for both heads.
+//   warp 0        TMA producer: the NH Q tiles once, then K/V tiles (plus the key tile's
+//                 dfs_in/dfs_out words) into a 2-stage ring;
+//   warp 1        allocates TMEM and issues every tcgen05.mma from one thread, head-interleaved:
+//                 O_i += P_i V(n-1), then S_i = Q_i K(n)^T, for i = 0..NH-1;
+//   warps 2+4i..  softmax warpgroup i (head i): thread r owns query row r (TMEM lane r), so the
+//                 row max and sum never leave the thread.  It reads S_i from TMEM, masks partial
+//                 tiles with dfs_in(node j) <= dfs_in(node i) <= dfs_out(node j) (and j <= i on
+//                 the diagonal tile), and writes P_i as bf16 back into the first half of S_i's
+//                 TMEM columns, where the P V MMA reads it as its A operand.
+// Online softmax per row, log2 units: m_ref is the offset O and l are scaled by.  It is moved
+// (and O rescaled in TMEM) only when the running max exceeds it by more than 8, so every P
+// value is at most 2^8; O / l is the same exact quotient whichever offset was used.  Two
+// partial states relate by the associative merge of the Tree Attention page.
 #include <cmath>
 
 #include "common.cuh"
@@ -22,26 +25,29 @@
 namespace ta {
 namespace {
 
-template <int HD>
+template <int HD, int NH>
 struct FwdCfg {
   static constexpr int NCH = HD / 64;                 // 64-column (128-byte) chunks per row
   static constexpr int NS = 2;                        // K/V ring stages
   static constexpr int Q_OFF = 0;
-  static constexpr int K_OFF = Q_OFF + NCH * CHUNK_BYTES;
+  static constexpr int K_OFF = Q_OFF + NH * NCH * CHUNK_BYTES;
   static constexpr int V_OFF = K_OFF + NS * NCH * CHUNK_BYTES;
-  static constexpr int P_OFF = V_OFF + NS * NCH * CHUNK_BYTES;
-  static constexpr int KIN_OFF = P_OFF + 2 * CHUNK_BYTES;
+  static constexpr int KIN_OFF = V_OFF + NS * NCH * CHUNK_BYTES;
   static constexpr int KOUT_OFF = KIN_OFF + NS * TILE * 4;
   static constexpr int BAR_OFF = KOUT_OFF + NS * TILE * 4;
-  static constexpr int NBAR = 1 + 2 * NS + 2 + 2 + 1 + 1 + 1;   // q, kv full/empty, s full/free, p, pv, drain
+  static constexpr int NBAR = 1 + 2 * NS + 3 * NH + 1;  // q, kv full/empty, s/p/o per head, drain
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int SMEM = MISC_OFF + 16;
   static constexpr int SMEM_ALLOC = SMEM + 1024;      // slack for 1024-byte alignment
-  static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t O_COL = 256;
+  static constexpr int THREADS = 64 + NH * 128;
+  // TMEM: S_i at columns 128 i (P_i packed bf16 in its first 64), O_i at 128 NH + HD i
+  static constexpr uint32_t O_COL0 = 128 * NH;
+  static constexpr uint32_t TMEM_NEED = 128 * NH + HD * NH;
+  static constexpr uint32_t TMEM_COLS = TMEM_NEED <= 256 ? 256 : 512;
   static constexpr uint32_t IDESC_S = idesc_bf16(TILE, TILE, 0, 0);   // Q K-major, K K-major
-  static constexpr uint32_t IDESC_PV = idesc_bf16(TILE, HD, 0, 1);    // P K-major, V MN-major
+  static constexpr uint32_t IDESC_PV = idesc_bf16(TILE, HD, 0, 1);    // P (TMEM) K-major, V MN-major
   static constexpr uint32_t KV_TX = 2 * NCH * CHUNK_BYTES + 2 * TILE * 4;
+  static constexpr float RESCALE_THRESHOLD = 8.f;     // log2 units
 };
 
 struct FwdParams {
@@ -54,12 +60,10 @@ struct FwdParams {
   __nv_bfloat16* o;
   float* lse;
   int32_t* status;
-  int N, T, Npad, Hq, grp;
+  int N, T, Npad, Hq, grp, n_hgroups;
   float scale_log2;          // softmax scale * log2(e)
   uint64_t wait_ns;
 };
-
-constexpr int kFwdThreads = 192;
 
 DEVI uint8_t* align1024(uint8_t* p) {
   const uint32_t a = smem_u32(p);
@@ -73,22 +77,21 @@ DEVI void mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
     if (global_timer_ns() - t0 > limit_ns) return;
 }
 
-template <int HD>
-__global__ void __launch_bounds__(kFwdThreads, 1)
+template <int HD, int NH>
+__global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
     k_attn_fwd(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-  using C = FwdCfg<HD>;
+  using C = FwdCfg<HD, NH>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::BAR_OFF);
   uint64_t* q_full = bars;
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = bars + 1 + C::NS;
-  uint64_t* s_full = bars + 1 + 2 * C::NS;
-  uint64_t* s_free = s_full + 2;
-  uint64_t* p_full = s_free + 2;
-  uint64_t* pv_done = p_full + 1;
-  uint64_t* drain = pv_done + 1;
+  uint64_t* s_full = bars + 1 + 2 * C::NS;            // [NH] S_i(n) computed (and PV_i(n-1) done)
+  uint64_t* p_full = s_full + NH;                     // [NH] P_i(n) in TMEM, O_i rescaled
+  uint64_t* o_done = p_full + NH;                     // [NH] last PV_i done
+  uint64_t* drain = o_done + NH;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::MISC_OFF);
   int* abort_flag = reinterpret_cast<int*>(sm + C::MISC_OFF + 4);
   int32_t* kin_s = reinterpret_cast<int32_t*>(sm + C::KIN_OFF);
@@ -96,18 +99,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u = blockIdx.x;
-  const int qt = p.row_order[u / p.Hq];
-  const int h = u % p.Hq;
-  const int kvh = h / p.grp;
+  const int qt = p.row_order[u / p.n_hgroups];
+  const int h0 = (u % p.n_hgroups) * NH;              // first q head of this CTA
+  const int kvh = h0 / p.grp;
   const int rp0 = p.row_ptr[qt];
   const int cnt = p.row_ptr[qt + 1] - rp0;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < C::NS; ++s) { mbar_init(&kv_full[s], 1); mbar_init(&kv_empty[s], 1); }
-    for (int b = 0; b < 2; ++b) { mbar_init(&s_full[b], 1); mbar_init(&s_free[b], 128); }
-    mbar_init(p_full, 128);
-    mbar_init(pv_done, 1);
+    for (int i = 0; i < NH; ++i) { mbar_init(&s_full[i], 1); mbar_init(&p_full[i], 128); mbar_init(&o_done[i], 1); }
     mbar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -128,8 +129,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
-      mbar_expect_tx(q_full, C::NCH * CHUNK_BYTES);
-      for (int c = 0; c < C::NCH; ++c) tma_load_3d(sm + C::Q_OFF + c * CHUNK_BYTES, &tmQ, q_full, c * 64, h, qt * TILE);
+      mbar_expect_tx(q_full, NH * C::NCH * CHUNK_BYTES);
+      for (int i = 0; i < NH; ++i)
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_3d(sm + C::Q_OFF + (i * C::NCH + c) * CHUNK_BYTES, &tmQ, q_full, c * 64, h0 + i, qt * TILE);
       int issued = 0;
       for (int n = 0; n < cnt; ++n) {
         const int s = n % C::NS;
@@ -155,142 +158,171 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t q_base = smem_u32(sm + C::Q_OFF);
-      const uint32_t p_base = smem_u32(sm + C::P_OFF);
-      auto issue_pv = [&](int m) -> bool {
-        const int s = m % C::NS;
-        if (!mbar_wait(p_full, m & 1, wc)) return false;
-        tc_fence_after();
-        const uint32_t v_base = smem_u32(sm + C::V_OFF + s * C::NCH * CHUNK_BYTES);
-#pragma unroll
-        for (int kk = 0; kk < TILE / 16; ++kk) {
-          const uint32_t a_off = (kk >> 2) * CHUNK_BYTES + (kk & 3) * 32;   // P: K-major, keys along K
-          const uint32_t b_off = kk * 16 * 128;                             // V: 16 key rows per step
-          umma_bf16(tmem + C::O_COL, sdesc_sw128(p_base + a_off, 16, 1024),
-                    sdesc_sw128(v_base + b_off, CHUNK_BYTES, 1024), C::IDESC_PV, (m > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(pv_done);
-        umma_commit(&kv_empty[s]);
-        return true;
-      };
-      bool ok = mbar_wait(q_full, 0, wc);
-      for (int n = 0; ok && n < cnt; ++n) {
-        const int s = n % C::NS, b = n & 1;
-        if (!mbar_wait(&kv_full[s], (n / C::NS) & 1, wc)) { ok = false; break; }
-        if (n >= 2 && !mbar_wait(&s_free[b], ((n >> 1) - 1) & 1, wc)) { ok = false; break; }
-        tc_fence_after();
+      auto issue_s = [&](int i, int s) {       // S_i = Q_i K(s)^T into TMEM columns 128 i
+        const uint32_t q_base = smem_u32(sm + C::Q_OFF + i * C::NCH * CHUNK_BYTES);
         const uint32_t k_base = smem_u32(sm + C::K_OFF + s * C::NCH * CHUNK_BYTES);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * CHUNK_BYTES + (kk & 3) * 32;     // d along K, 32 B per step
-          umma_bf16(tmem + b * TILE, sdesc_sw128(q_base + off, 16, 1024), sdesc_sw128(k_base + off, 16, 1024),
+          const uint32_t off = (kk >> 2) * CHUNK_BYTES + (kk & 3) * 32;   // d along K, 32 B per step
+          umma_bf16(tmem + 128 * i, sdesc_sw128(q_base + off, 16, 1024), sdesc_sw128(k_base + off, 16, 1024),
                     C::IDESC_S, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&s_full[b]);
-        if (n >= 1 && !issue_pv(n - 1)) { ok = false; break; }
+        umma_commit(&s_full[i]);
+      };
+      auto issue_pv = [&](int i, int m) -> bool {   // O_i += P_i(m) V(m)
+        if (!mbar_wait(&p_full[i], m & 1, wc)) return false;
+        tc_fence_after();
+        const uint32_t v_base = smem_u32(sm + C::V_OFF + (m % C::NS) * C::NCH * CHUNK_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < TILE / 16; ++kk)     // 16 keys per step: 8 TMEM columns of P, 16 V rows
+          umma_bf16_tmem_a(tmem + C::O_COL0 + HD * i, tmem + 128 * i + kk * 8,
+                           sdesc_sw128(v_base + kk * 16 * 128, CHUNK_BYTES, 1024), C::IDESC_PV,
+                           (m > 0 || kk > 0) ? 1u : 0u);
+        return true;
+      };
+      bool ok = mbar_wait(q_full, 0, wc) && (cnt == 0 || mbar_wait(&kv_full[0], 0, wc));
+      if (ok && cnt > 0) {
+        tc_fence_after();
+        for (int i = 0; i < NH; ++i) issue_s(i, 0);
       }
-      if (ok && cnt > 0) issue_pv(cnt - 1);
+      for (int n = 1; ok && n < cnt; ++n) {
+        const int s = n % C::NS;
+        if (!mbar_wait(&kv_full[s], (n / C::NS) & 1, wc)) { ok = false; break; }
+        tc_fence_after();
+        for (int i = 0; ok && i < NH; ++i) {
+          if (!issue_pv(i, n - 1)) { ok = false; break; }
+          if (i == NH - 1) umma_commit(&kv_empty[(n - 1) % C::NS]);
+          issue_s(i, s);                       // overwrites S_i / P_i: ordered after PV_i(n-1)
+        }
+      }
+      if (ok && cnt > 0) {
+        for (int i = 0; ok && i < NH; ++i) {
+          if (!issue_pv(i, cnt - 1)) { ok = false; break; }
+          umma_commit(&o_done[i]);
+        }
+        umma_commit(&kv_empty[(cnt - 1) % C::NS]);
+      }
       umma_commit(drain);                      // completes once every MMA above is done
       mbar_wait_drain(drain, 0, p.wait_ns);
     }
   } else {
-    // ---------------------------------------------------------------- softmax warps
+    // ---------------------------------------------------------------- softmax warpgroups
+    const int wg = (warp - 2) >> 2;            // head index inside the CTA
     const int wq = warp & 3;                   // TMEM lane quarter this warp may access
     const int r = wq * 32 + lane;              // query row inside the tile
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t s_addr = tmem + lane_off + 128 * wg;
+    const uint32_t o_addr = tmem + lane_off + C::O_COL0 + HD * wg;
+    const int h = h0 + wg;
     const int qi = qt * TILE + r;
     const int qin = p.tok_in[qi];
+    const float sl2 = p.scale_log2;
+    const uint64_t sl2x2 = f2_pack(sl2, sl2);
     float m_run = -INFINITY;                   // running row max (log2 units)
-    float m_ref = 0.f;                         // offset the current O and l are scaled by
+    float m_ref = 0.f;                         // offset O and l are currently scaled by
     float l_run = 0.f;
     bool ok = true;
     for (int n = 0; n < cnt; ++n) {
-      const int b = n & 1, s = n % C::NS;
+      const int s = n % C::NS;
       const int kt = p.row_idx[rp0 + n];
       const uint8_t cls = p.tile_class[(size_t)qt * p.T + kt];
-      if (!mbar_wait_warp(&s_full[b], (n >> 1) & 1, wc)) { ok = false; break; }
+      if (!mbar_wait_warp(&s_full[wg], n & 1, wc)) { ok = false; break; }
       tc_fence_after();
-      float sv[TILE];
-#pragma unroll
-      for (int j = 0; j < TILE / 32; ++j) {
-        uint32_t rr[32];
-        tmem_load32(lane_base + b * TILE + j * 32, rr);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) sv[j * 32 + c] = __uint_as_float(rr[c]);
-      }
-      tc_fence_before();
-      mbar_arrive(&s_free[b]);
+      uint32_t sv[TILE];
+      tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(sv + 0));
+      tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+      tmem_ld32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(sv + 64));
+      tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(sv + 96));
+      tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(sv + 0));
+      tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+      tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(sv + 64));
+      tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(sv + 96));
       if (cls == 1) {                          // partial tile: tree mask in registers
         if (!mbar_wait_warp(&kv_full[s], (n / C::NS) & 1, wc)) { ok = false; break; }
         const int4* kin4 = reinterpret_cast<const int4*>(kin_s + s * TILE);
         const int4* kout4 = reinterpret_cast<const int4*>(kout_s + s * TILE);
+        const uint32_t ninf = __float_as_uint(-INFINITY);
         const int jrel = qi - kt * TILE;       // key c is causal-visible iff c <= jrel
 #pragma unroll
         for (int c4 = 0; c4 < TILE / 4; ++c4) {
           const int4 a = kin4[c4], z = kout4[c4];
           const int c = c4 * 4;
-          if (!(c + 0 <= jrel && a.x <= qin && qin <= z.x)) sv[c + 0] = -INFINITY;
-          if (!(c + 1 <= jrel && a.y <= qin && qin <= z.y)) sv[c + 1] = -INFINITY;
-          if (!(c + 2 <= jrel && a.z <= qin && qin <= z.z)) sv[c + 2] = -INFINITY;
-          if (!(c + 3 <= jrel && a.w <= qin && qin <= z.w)) sv[c + 3] = -INFINITY;
+          if (!(c + 0 <= jrel && a.x <= qin && qin <= z.x)) sv[c + 0] = ninf;
+          if (!(c + 1 <= jrel && a.y <= qin && qin <= z.y)) sv[c + 1] = ninf;
+          if (!(c + 2 <= jrel && a.z <= qin && qin <= z.z)) sv[c + 2] = ninf;
+          if (!(c + 3 <= jrel && a.w <= qin && qin <= z.w)) sv[c + 3] = ninf;
         }
       }
-      float mx[8];
+      float mx[4];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) mx[e] = sv[e];
+      for (int e = 0; e < 4; ++e) mx[e] = __uint_as_float(sv[e]);
 #pragma unroll
-      for (int c = 8; c < TILE; ++c) mx[c & 7] = fmaxf(mx[c & 7], sv[c]);
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      const float m_new = fmaxf(m_run, mt * p.scale_log2);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = (l_run == 0.f) ? 0.f : ex2_approx(m_ref - m_use);
-      uint32_t pk[TILE / 2];
-      float rs[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int c = 4; c < TILE; c += 8)
 #pragma unroll
-      for (int c = 0; c < TILE; c += 2) {
-        const float p0 = ex2_approx(fmaf(sv[c], p.scale_log2, -m_use));
-        const float p1 = ex2_approx(fmaf(sv[c + 1], p.scale_log2, -m_use));
-        rs[(c >> 1) & 3] += p0 + p1;
-        pk[c >> 1] = pack_bf16(p0, p1);
-      }
-      l_run = l_run * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
-      if (n > 0) {
-        if (!mbar_wait_warp(pv_done, (n - 1) & 1, wc)) { ok = false; break; }
-        tc_fence_after();
-        // TMEM ld/st are warp-collective: rescale when any row of the warp needs it
-        // (rows whose max did not move have alpha == 1 and are multiplied exactly by 1)
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-          for (int j = 0; j < HD / 32; ++j) {
-            uint32_t rr[32];
-            tmem_load32(lane_base + C::O_COL + j * 32, rr);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) rr[c] = __float_as_uint(__uint_as_float(rr[c]) * alpha);
-            tmem_store32(lane_base + C::O_COL + j * 32, rr);
-          }
-          tmem_wait_st();
-        }
-      }
-      uint8_t* pbox = sm + C::P_OFF;
-#pragma unroll
-      for (int uu = 0; uu < TILE / 8; ++uu)
-        st_swizzled_unit(pbox + (uu >> 3) * CHUNK_BYTES, r, uu & 7,
-                         make_uint4(pk[4 * uu], pk[4 * uu + 1], pk[4 * uu + 2], pk[4 * uu + 3]));
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(p_full);
+        for (int e = 0; e < 4; ++e)
+          mx[e] = fmax3(mx[e], __uint_as_float(sv[c + 2 * e]), __uint_as_float(sv[c + 2 * e + 1]));
+      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      const float m_new = fmaxf(m_run, mt * sl2);
       m_run = m_new;
-      m_ref = m_use;
+      float alpha = 1.f;
+      if (l_run == 0.f) {                      // nothing accumulated yet: take the offset as is
+        m_ref = (m_new == -INFINITY) ? 0.f : m_new;
+      } else if (m_new > m_ref + C::RESCALE_THRESHOLD) {
+        alpha = ex2_approx(m_ref - m_new);
+        m_ref = m_new;
+      }
+      const uint64_t negm = f2_pack(-m_ref, -m_ref);
+      uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
+      // P_i over the first 64 columns of S_i (S_i is already in registers): 64 scores per half
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 64 * half; c < 64 * half + 64; c += 4) {
+          float x0, x1, x2, x3;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2x2, negm), x0, x1);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), sl2x2, negm), x2, x3);
+          const float e0 = ex2_approx(x0), e1 = ex2_approx(x1), e2 = ex2_approx(x2), e3 = ex2_approx(x3);
+          acc0 = f2_add(acc0, f2_pack(e0, e1));
+          acc1 = f2_add(acc1, f2_pack(e2, e3));
+          pk[(c - 64 * half) >> 1] = pack_bf16(e0, e1);
+          pk[((c - 64 * half) >> 1) + 1] = pack_bf16(e2, e3);
+        }
+        tmem_store32(s_addr + 32 * half, pk);
+      }
+      float a0, a1, a2, a3;
+      f2_unpack(acc0, a0, a1);
+      f2_unpack(acc1, a2, a3);
+      l_run = l_run * alpha + ((a0 + a1) + (a2 + a3));
+      // S_i(n) complete implies PV_i(n-1) complete: O_i is stable here
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {
+        const uint64_t al = f2_pack(alpha, alpha);
+#pragma unroll 1
+        for (int j = 0; j < HD / 32; ++j) {
+          uint32_t rr[32];
+          tmem_load32(o_addr + j * 32, rr);
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            float y0, y1;
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(rr[c]), __uint_as_float(rr[c + 1])), al), y0, y1);
+            rr[c] = __float_as_uint(y0);
+            rr[c + 1] = __float_as_uint(y1);
+          }
+          tmem_store32(o_addr + j * 32, rr);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&p_full[wg]);
     }
-    if (ok && cnt > 0 && mbar_wait_warp(pv_done, (cnt - 1) & 1, wc)) {
+    if (ok && cnt > 0 && mbar_wait_warp(&o_done[wg], 0, wc)) {
       tc_fence_after();
       const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
       __nv_bfloat16* orow = p.o + ((size_t)qi * p.Hq + h) * HD;
-#pragma unroll
+#pragma unroll 1
       for (int j = 0; j < HD / 32; ++j) {
         uint32_t rr[32];
-        tmem_load32(lane_base + C::O_COL + j * 32, rr);
+        tmem_load32(o_addr + j * 32, rr);
         if (qi < p.N) {
           uint4* dst = reinterpret_cast<uint4*>(orow + j * 32);
 #pragma unroll
@@ -304,7 +336,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
         }
       }
-      p.lse[(size_t)h * p.Npad + qi] = (qi < p.N && l_run > 0.f) ? (m_ref + log2f(l_run)) * 0.69314718055994531f : 0.f;
+      p.lse[(size_t)h * p.Npad + qi] =
+          (qi < p.N && l_run > 0.f) ? (m_ref + log2f(l_run)) * 0.69314718055994531f : 0.f;
     }
   }
   // ---------------------------------------------------------------- teardown
@@ -317,22 +350,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
-template <int HD>
-int launch_fwd(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k, const tree_bf16* v, int Hq,
+template <int HD, int NH>
+int launch_fwd(const tree_plan_t* plan, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, int Hq,
                int Hkv, float scale, tree_bf16* o, float* lse, int32_t* status, cudaStream_t s) {
-  using C = FwdCfg<HD>;
+  using C = FwdCfg<HD, NH>;
   const int N = plan->n_tokens, T = plan->n_tiles;
-  CUtensorMap tq, tk, tv;
-  int rc = make_tmap_bf16_3d(&tq, q, HD, Hq, N);
-  if (!rc) rc = make_tmap_bf16_3d(&tk, k, HD, Hkv, N);
-  if (!rc) rc = make_tmap_bf16_3d(&tv, v, HD, Hkv, N);
-  if (rc) return rc;
-  rc = record_cuda(cudaFuncSetAttribute(k_attn_fwd<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC));
+  int rc = record_cuda(
+      cudaFuncSetAttribute(k_attn_fwd<HD, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC));
   if (rc) return rc;
   FwdParams P{plan->row_ptr, plan->row_idx, plan->row_order, plan->tok_in, plan->tok_out, plan->tile_class,
-              reinterpret_cast<__nv_bfloat16*>(o), lse, status, N, T, T * TILE, Hq, Hq / Hkv,
+              reinterpret_cast<__nv_bfloat16*>(o), lse, status, N, T, T * TILE, Hq, Hq / Hkv, Hq / NH,
               scale * 1.4426950408889634f, wait_limit_ns()};
-  k_attn_fwd<HD><<<T * Hq, kFwdThreads, C::SMEM_ALLOC, s>>>(tq, tk, tv, P);
+  k_attn_fwd<HD, NH><<<T * (Hq / NH), C::THREADS, C::SMEM_ALLOC, s>>>(tq, tk, tv, P);
   return record_cuda(cudaGetLastError());
 }
 
@@ -353,6 +382,16 @@ extern "C" int tree_attn_fwd(const tree_plan_t* plan, const tree_bf16* q, const 
   if (rc) return rc;
   if (!(scale > 0.f)) scale = 1.f / sqrtf(static_cast<float>(d));
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return d == 128 ? launch_fwd<128>(plan, q, k, v, Hq, Hkv, scale, o, lse, status_dev, s)
-                  : launch_fwd<64>(plan, q, k, v, Hq, Hkv, scale, o, lse, status_dev, s);
+  const int N = plan->n_tokens;
+  CUtensorMap tq, tk, tv;
+  rc = make_tmap_bf16_3d(&tq, q, d, Hq, N);
+  if (!rc) rc = make_tmap_bf16_3d(&tk, k, d, Hkv, N);
+  if (!rc) rc = make_tmap_bf16_3d(&tv, v, d, Hkv, N);
+  if (rc) return rc;
+  const bool pair = ((Hq / Hkv) % 2) == 0;   // two q heads of one kv group per CTA
+  if (d == 128)
+    return pair ? launch_fwd<128, 2>(plan, tq, tk, tv, Hq, Hkv, scale, o, lse, status_dev, s)
+                : launch_fwd<128, 1>(plan, tq, tk, tv, Hq, Hkv, scale, o, lse, status_dev, s);
+  return pair ? launch_fwd<64, 2>(plan, tq, tk, tv, Hq, Hkv, scale, o, lse, status_dev, s)
+              : launch_fwd<64, 1>(plan, tq, tk, tv, Hq, Hkv, scale, o, lse, status_dev, s);
 }
