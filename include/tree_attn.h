@@ -52,7 +52,8 @@ enum {
   TREE_ERR_ARCH = -3,         /* current device is not compute capability 10.3 */
   TREE_ERR_CUDA = -4,         /* a CUDA runtime call or launch failed */
   TREE_ERR_TIMEOUT = -5,      /* a bounded device wait expired (written to status_dev) */
-  TREE_ERR_ARG = -6           /* NULL or misaligned pointer, bad size */
+  TREE_ERR_ARG = -6,          /* NULL or misaligned pointer, bad size */
+  TREE_ERR_SCRATCH = -7       /* problem needs more scratch than tree_attn_bwd_noalloc holds */
 };
 
 /* ---------------------------------------------------------------------------------------
@@ -167,6 +168,32 @@ int tree_attn_bwd(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* 
                   const tree_bf16* dO, int Hq, int Hkv, int d, float scale, float rope_theta,
                   void* workspace, tree_bf16* dq, tree_bf16* dk, tree_bf16* dv,
                   int32_t* status_dev, tree_stream_t stream);
+
+/* Backward without any allocation by the caller or the library (this entry point has no
+ * counterpart in the Tree Training explainer; it exists for callers).  Some callers cannot
+ * provide the workspace tree_attn_bwd needs: code that drives this library through the plain
+ * C ABI from a host runtime which owns every device allocation and forbids new ones after
+ * start-up (fixed memory budgets), or that must not pay cudaMalloc's implicit device
+ * synchronisation on its path.  This variant takes the delta / fp32 dQ scratch from one
+ * fixed array of TREE_NOALLOC_SCRATCH_BYTES (64 MiB) compiled into the library as device
+ * memory; every GPU that loads the library holds that array until the process exits.
+ * Same arguments and results as tree_attn_bwd, minus `workspace`.
+ *   - Size limit: a problem whose tree_attn_bwd_workspace() exceeds the array is rejected
+ *     with TREE_ERR_SCRATCH before anything is launched (at d = 128, Hq = 32 that is about
+ *     4000 tokens).
+ *   - Set-up: the first call on each device looks up the array's device address (with that
+ *     device current) and caches it; make that first call before any stream capture.
+ *   - Sharing: every call on a device uses the same array, which keeps the last call's
+ *     contents (the accumulator is cleared at the start of each call).  Calls that overlap
+ *     on the GPU (different streams, or different host threads without ordering) race on
+ *     it and corrupt each other's gradients: serialise them.
+ *   - It calls no cudaMalloc / cudaFree and no allocating library routine. */
+#define TREE_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+int tree_attn_bwd_noalloc(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k,
+                          const tree_bf16* v, const tree_bf16* o, const float* lse,
+                          const tree_bf16* dO, int Hq, int Hkv, int d, float scale,
+                          float rope_theta, tree_bf16* dq, tree_bf16* dk, tree_bf16* dv,
+                          int32_t* status_dev, tree_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
  * Diagnostics

@@ -491,3 +491,52 @@ extern "C" int tree_attn_bwd(const tree_plan_t* plan, const tree_bf16* q, const 
                   : launch_bwd<64>(plan, q, k, v, o, lse, dO, Hq, Hkv, scale, rope_theta, workspace, dq, dk, dv,
                                    status_dev, s);
 }
+
+// ------------------------------------------------------------------------------------------
+// Non-allocating backward: the same kernels, with the delta / dQ-accumulator scratch taken
+// from one fixed device array instead of a caller workspace (for callers that cannot
+// allocate device memory).  The array is shared by every call on a device; the accumulator
+// is zeroed at the start of each call, and overlapping calls race on it.
+#include <mutex>
+
+namespace ta {
+namespace {
+static __device__ __align__(256) unsigned char g_noalloc_scratch[TREE_NOALLOC_SCRATCH_BYTES];
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[64];            // device address of the array, per device ordinal
+
+// Looks the array's address up once per device, with that device current.
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  int rc = record_cuda(cudaGetDevice(&dev));
+  if (rc) return rc;
+  if (dev < 0 || dev >= 64) return TREE_ERR_ARG;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    rc = record_cuda(cudaGetSymbolAddress(&p, g_noalloc_scratch));
+    if (rc) return rc;
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return TREE_OK;
+}
+}  // namespace
+}  // namespace ta
+
+extern "C" int tree_attn_bwd_noalloc(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k,
+                                     const tree_bf16* v, const tree_bf16* o, const float* lse, const tree_bf16* dO,
+                                     int Hq, int Hkv, int d, float scale, float rope_theta, tree_bf16* dq,
+                                     tree_bf16* dk, tree_bf16* dv, int32_t* status_dev, tree_stream_t stream) {
+  int rc = plan_ok(plan);
+  if (rc) return rc;
+  if ((d != 64 && d != 128) || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return TREE_ERR_SHAPE;
+  if (tree_attn_bwd_workspace(plan, Hq, d) > TREE_NOALLOC_SCRATCH_BYTES) return TREE_ERR_SCRATCH;
+  rc = check_device();
+  if (rc) return rc;
+  void* scratch = nullptr;
+  rc = noalloc_scratch(&scratch);
+  if (rc) return rc;
+  return tree_attn_bwd(plan, q, k, v, o, lse, dO, Hq, Hkv, d, scale, rope_theta, scratch, dq, dk, dv, status_dev,
+                       stream);
+}

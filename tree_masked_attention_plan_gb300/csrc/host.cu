@@ -144,6 +144,7 @@ const char* tree_strerror(int code) {
     case TREE_ERR_CUDA: return "CUDA runtime error (see tree_last_cuda_error)";
     case TREE_ERR_TIMEOUT: return "a bounded device wait expired";
     case TREE_ERR_ARG: return "null or misaligned pointer, or bad size";
+    case TREE_ERR_SCRATCH: return "problem needs more scratch than the non-allocating backward's fixed array";
     default: return "unknown error code";
   }
 }
