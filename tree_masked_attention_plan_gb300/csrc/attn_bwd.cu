@@ -22,7 +22,7 @@
 namespace ta {
 namespace {
 
-constexpr int kBwdThreads = 192;
+constexpr int kMaxList = 1024;      // column lists up to this length are staged in shared memory
 
 template <int HD>
 struct BwdCfg {
@@ -31,20 +31,23 @@ struct BwdCfg {
   static constexpr int V_OFF = K_OFF + NCH * CHUNK_BYTES;
   static constexpr int Q_OFF = V_OFF + NCH * CHUNK_BYTES;
   static constexpr int DO_OFF = Q_OFF + NCH * CHUNK_BYTES;
-  static constexpr int PT_OFF = DO_OFF + NCH * CHUNK_BYTES;
-  static constexpr int DST_OFF = PT_OFF + 2 * CHUNK_BYTES;
+  static constexpr int DST_OFF = DO_OFF + NCH * CHUNK_BYTES;
   static constexpr int LSE_OFF = DST_OFF + 2 * CHUNK_BYTES;
   static constexpr int DLT_OFF = LSE_OFF + TILE * 4;
   static constexpr int QIN_OFF = DLT_OFF + TILE * 4;
-  static constexpr int BAR_OFF = QIN_OFF + TILE * 4;
+  static constexpr int LIST_OFF = QIN_OFF + TILE * 4;           // int32 query tiles of the column
+  static constexpr int LCLS_OFF = LIST_OFF + kMaxList * 4;     // uint8 their tile classes
+  static constexpr int BAR_OFF = LCLS_OFF + kMaxList;
   static constexpr int NBAR = 9;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int SMEM = MISC_OFF + 16;
   static constexpr int SMEM_ALLOC = SMEM + 1024;
+  static constexpr int THREADS = 64 + 256;                      // producer, MMA, 8 elementwise warps
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t ST_COL = 0, DPT_COL = 128, DV_COL = 256, DK_COL = 256 + HD, DQ_COL = 0;
+  // TMEM columns: S^T in A (P^T packed bf16 over it, query half g at 64 g), dP^T and dQ in B
+  static constexpr uint32_t A_COL = 0, B_COL = 128, DV_COL = 256, DK_COL = 256 + HD;
   static constexpr uint32_t IDESC_SDP = idesc_bf16(TILE, TILE, 0, 0);   // K/V K-major, Q/dO K-major
-  static constexpr uint32_t IDESC_DKV = idesc_bf16(TILE, HD, 0, 1);     // P^T/dS^T K-major, dO/Q MN-major
+  static constexpr uint32_t IDESC_DKV = idesc_bf16(TILE, HD, 0, 1);     // P^T (TMEM) / dS^T K-major, dO/Q MN-major
   static constexpr uint32_t IDESC_DQ = idesc_bf16(TILE, HD, 1, 1);      // dS MN-major, K MN-major
   static constexpr uint32_t KV_TX = 2 * NCH * CHUNK_BYTES;
   static constexpr uint32_t QDO_TX = 2 * NCH * CHUNK_BYTES + 3 * TILE * 4;
@@ -113,7 +116,7 @@ __global__ void k_zero_f32x4(float4* p, size_t n4) {
 
 // ------------------------------------------------------------------------------------------
 template <int HD>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
     k_bwd_dkdv(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                const BwdParams p) {
@@ -132,9 +135,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* drain = bars + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::MISC_OFF);
   int* abort_flag = reinterpret_cast<int*>(sm + C::MISC_OFF + 4);
-  float* lse_s = reinterpret_cast<float*>(sm + C::LSE_OFF);
-  float* dlt_s = reinterpret_cast<float*>(sm + C::DLT_OFF);
-  int32_t* qin_s = reinterpret_cast<int32_t*>(sm + C::QIN_OFF);
+  const float* lse_s = reinterpret_cast<const float*>(sm + C::LSE_OFF);
+  const float* dlt_s = reinterpret_cast<const float*>(sm + C::DLT_OFF);
+  const int32_t* qin_s = reinterpret_cast<const int32_t*>(sm + C::QIN_OFF);
+  int32_t* list_s = reinterpret_cast<int32_t*>(sm + C::LIST_OFF);
+  uint8_t* lcls_s = sm + C::LCLS_OFF;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u = blockIdx.x;
@@ -142,16 +147,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int kvh = u % p.Hkv;
   const int cp0 = p.col_ptr[kt];
   const int ccnt = p.col_ptr[kt + 1] - cp0;
-  const int total = ccnt * p.grp;               // steps: q head (outer) x query tile (inner)
+  const int total = ccnt * p.grp;               // steps: q head (outer) x query tile (inner, descending)
+
+  // the column's query tiles and their classes, staged once
+  for (int i = threadIdx.x; i < ccnt && i < kMaxList; i += blockDim.x) {
+    const int qt = p.col_idx[cp0 + i];
+    list_s[i] = qt;
+    lcls_s[i] = p.tile_class[(size_t)qt * p.T + kt];
+  }
+  // step n -> (q head, query tile, class); tiles are taken from the end of the column so that
+  // the CTAs running at one time work on the same query tiles (their dQ lines stay in L2)
+  auto step_tile = [&](int n, int& h, int& qt, int& cls) {
+    const int i = ccnt - 1 - n % ccnt;
+    h = kvh * p.grp + n / ccnt;
+    if (i < kMaxList) { qt = list_s[i]; cls = lcls_s[i]; }
+    else { qt = p.col_idx[cp0 + i]; cls = p.tile_class[(size_t)qt * p.T + kt]; }
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
     mbar_init(qdo_full, 1);
     mbar_init(qdo_empty, 1);
     mbar_init(sdp_full, 1);
-    mbar_init(ds_ready, 128);
+    mbar_init(ds_ready, 256);
     mbar_init(dq_full, 1);
-    mbar_init(dq_free, 128);
+    mbar_init(dq_free, 256);
     mbar_init(dkdv_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -181,8 +201,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       int issued = 0;
       for (int n = 0; n < total; ++n) {
-        const int h = kvh * p.grp + n / ccnt;
-        const int qt = p.col_idx[cp0 + n % ccnt];
+        int h, qt, cls;
+        step_tile(n, h, qt, cls);
         if (n > 0 && !mbar_wait(qdo_empty, (n - 1) & 1, wc)) break;
         mbar_expect_tx(qdo_full, C::QDO_TX);
         for (int c = 0; c < C::NCH; ++c) {
@@ -190,9 +210,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tma_load_3d(sm + C::DO_OFF + c * CHUNK_BYTES, &tmDO, qdo_full, c * 64, h, qt * TILE);
         }
         const size_t lo = (size_t)h * p.Npad + (size_t)qt * TILE;
-        bulk_load(lse_s, p.lse + lo, TILE * 4, qdo_full);
-        bulk_load(dlt_s, p.dlt + lo, TILE * 4, qdo_full);
-        bulk_load(qin_s, p.tok_in + (size_t)qt * TILE, TILE * 4, qdo_full);
+        bulk_load(sm + C::LSE_OFF, p.lse + lo, TILE * 4, qdo_full);
+        bulk_load(sm + C::DLT_OFF, p.dlt + lo, TILE * 4, qdo_full);
+        bulk_load(sm + C::QIN_OFF, p.tok_in + (size_t)qt * TILE, TILE * 4, qdo_full);
         issued = n + 1;
       }
       if (*abort_flag) {
@@ -205,45 +225,47 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0) {
       const uint32_t k_base = smem_u32(sm + C::K_OFF), v_base = smem_u32(sm + C::V_OFF);
       const uint32_t q_base = smem_u32(sm + C::Q_OFF), do_base = smem_u32(sm + C::DO_OFF);
-      const uint32_t pt_base = smem_u32(sm + C::PT_OFF), dst_base = smem_u32(sm + C::DST_OFF);
+      const uint32_t dst_base = smem_u32(sm + C::DST_OFF);
       bool ok = mbar_wait(kv_full, 0, wc);
       for (int n = 0; ok && n < total; ++n) {
         if (!mbar_wait(qdo_full, n & 1, wc)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {                 // S^T = K Q^T into A (after dV(n-1) read P^T)
+          const uint32_t off = (kk >> 2) * CHUNK_BYTES + (kk & 3) * 32;
+          umma_bf16(tmem + C::A_COL, sdesc_sw128(k_base + off, 16, 1024), sdesc_sw128(q_base + off, 16, 1024),
+                    C::IDESC_SDP, kk > 0 ? 1u : 0u);
+        }
         if (n > 0 && !mbar_wait(dq_free, (n - 1) & 1, wc)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {                 // S^T = K Q^T, dP^T = V dO^T
+        for (int kk = 0; kk < HD / 16; ++kk) {                 // dP^T = V dO^T into B (dQ(n-1) drained)
           const uint32_t off = (kk >> 2) * CHUNK_BYTES + (kk & 3) * 32;
-          umma_bf16(tmem + C::ST_COL, sdesc_sw128(k_base + off, 16, 1024), sdesc_sw128(q_base + off, 16, 1024),
-                    C::IDESC_SDP, kk > 0 ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * CHUNK_BYTES + (kk & 3) * 32;
-          umma_bf16(tmem + C::DPT_COL, sdesc_sw128(v_base + off, 16, 1024), sdesc_sw128(do_base + off, 16, 1024),
+          umma_bf16(tmem + C::B_COL, sdesc_sw128(v_base + off, 16, 1024), sdesc_sw128(do_base + off, 16, 1024),
                     C::IDESC_SDP, kk > 0 ? 1u : 0u);
         }
         umma_commit(sdp_full);
         if (!mbar_wait(ds_ready, n & 1, wc)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < TILE / 16; ++kk) {               // dV += P^T dO, dK += dS^T Q
+        for (int kk = 0; kk < TILE / 16; ++kk) {               // dV += P^T dO (P^T from TMEM), dK += dS^T Q
+          const uint32_t a_col = C::A_COL + (kk >> 2) * 64 + (kk & 3) * 8;
           const uint32_t a_off = (kk >> 2) * CHUNK_BYTES + (kk & 3) * 32;
           const uint32_t b_off = kk * 16 * 128;
           const uint32_t acc = (n > 0 || kk > 0) ? 1u : 0u;
-          umma_bf16(tmem + C::DV_COL, sdesc_sw128(pt_base + a_off, 16, 1024),
-                    sdesc_sw128(do_base + b_off, CHUNK_BYTES, 1024), C::IDESC_DKV, acc);
+          umma_bf16_tmem_a(tmem + C::DV_COL, tmem + a_col, sdesc_sw128(do_base + b_off, CHUNK_BYTES, 1024),
+                           C::IDESC_DKV, acc);
           umma_bf16(tmem + C::DK_COL, sdesc_sw128(dst_base + a_off, 16, 1024),
                     sdesc_sw128(q_base + b_off, CHUNK_BYTES, 1024), C::IDESC_DKV, acc);
         }
+        umma_commit(qdo_empty);                                  // Q, dO, LSE, delta free: next load starts
 #pragma unroll
-        for (int kk = 0; kk < TILE / 16; ++kk) {               // dQ = dS K  (keys along K)
+        for (int kk = 0; kk < TILE / 16; ++kk) {               // dQ = dS K into B (keys along K)
           const uint32_t off = kk * 16 * 128;
-          umma_bf16(tmem + C::DQ_COL, sdesc_sw128(dst_base + off, CHUNK_BYTES, 1024),
+          umma_bf16(tmem + C::B_COL, sdesc_sw128(dst_base + off, CHUNK_BYTES, 1024),
                     sdesc_sw128(k_base + off, CHUNK_BYTES, 1024), C::IDESC_DQ, kk > 0 ? 1u : 0u);
         }
         umma_commit(dq_full);
-        umma_commit(qdo_empty);
       }
       if (ok) umma_commit(dkdv_done);
       umma_commit(drain);
@@ -251,55 +273,61 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else {
     // ---------------------------------------------------------------- elementwise warps
+    // Two warpgroups share the 128 TMEM lanes: group g takes query columns [64 g, 64 g + 64)
+    // of S^T / dP^T, and output columns [HD/2 g, HD/2 (g+1)) of dQ and dV.
+    const int g = (warp - 2) >> 2;
     const int wq = warp & 3;
-    const int r = wq * 32 + lane;                 // key row for S^T/dP^T/dK/dV, query row for dQ
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const int r = wq * 32 + lane;                 // key row (S^T, dP^T, dK, dV) or query row (dQ)
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const int j = kt * TILE + r;
     const int kin = p.tok_in[j], kout = p.tok_out[j];
     const float nl2e = -1.4426950408889634f;
     bool ok = true;
     for (int n = 0; n < total; ++n) {
-      const int h = kvh * p.grp + n / ccnt;
-      const int qt = p.col_idx[cp0 + n % ccnt];
-      const uint8_t cls = p.tile_class[(size_t)qt * p.T + kt];
+      int h, qt, cls;
+      step_tile(n, h, qt, cls);
       if (!mbar_wait_warp(qdo_full, n & 1, wc) || !mbar_wait_warp(sdp_full, n & 1, wc)) { ok = false; break; }
       tc_fence_after();
       const int jrel = j - qt * TILE;             // query i is causal-visible iff i >= jrel
 #pragma unroll 1
-      for (int jc = 0; jc < TILE / 32; ++jc) {
+      for (int jc = 0; jc < 2; ++jc) {
+        const int c0 = 64 * g + 32 * jc;          // first query column of this 32-wide chunk
         uint32_t sr[32], dr[32];
-        tmem_ld32(lane_base + C::ST_COL + jc * 32, sr);
-        tmem_ld32(lane_base + C::DPT_COL + jc * 32, dr);
+        tmem_ld32(tmem + lane_off + C::A_COL + c0, sr);
+        tmem_ld32(tmem + lane_off + C::B_COL + c0, dr);
         tmem_wait_ld(sr);
         tmem_wait_ld(dr);
         uint32_t pp[16], dd[16];
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float pv[2], dv_[2];
+        for (int c = 0; c < 32; c += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(lse_s + c0 + c);
+          const float4 d4 = *reinterpret_cast<const float4*>(dlt_s + c0 + c);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dl[4] = {d4.x, d4.y, d4.z, d4.w};
+          float pv[4], dsv[4];
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int i = jc * 32 + c + e;
-            float pe = ex2_approx(fmaf(__uint_as_float(sr[c + e]), p.scale_log2, lse_s[i] * nl2e));
+          for (int e = 0; e < 4; ++e) {
+            float pe = ex2_approx(fmaf(__uint_as_float(sr[c + e]), p.scale_log2, lv[e] * nl2e));
             if (cls == 1) {
+              const int i = c0 + c + e;
               const int qi_in = qin_s[i];
-              const bool vis = (i >= jrel) && (kin <= qi_in) && (qi_in <= kout);
-              pe = vis ? pe : 0.f;
+              pe = ((i >= jrel) && (kin <= qi_in) && (qi_in <= kout)) ? pe : 0.f;
             }
             pv[e] = pe;
-            dv_[e] = pe * (__uint_as_float(dr[c + e]) - dlt_s[i]) * p.scale;
+            dsv[e] = pe * (__uint_as_float(dr[c + e]) - dl[e]) * p.scale;
           }
           pp[c >> 1] = pack_bf16(pv[0], pv[1]);
-          dd[c >> 1] = pack_bf16(dv_[0], dv_[1]);
+          pp[(c >> 1) + 1] = pack_bf16(pv[2], pv[3]);
+          dd[c >> 1] = pack_bf16(dsv[0], dsv[1]);
+          dd[(c >> 1) + 1] = pack_bf16(dsv[2], dsv[3]);
         }
-        uint8_t* ptb = sm + C::PT_OFF + (jc >> 1) * CHUNK_BYTES;
-        uint8_t* dsb = sm + C::DST_OFF + (jc >> 1) * CHUNK_BYTES;
+        // P^T for these 32 queries: 16 packed columns inside this group's own S^T columns
+        tmem_store16(tmem + lane_off + C::A_COL + 64 * g + 16 * jc, pp);
+        uint8_t* dsb = sm + C::DST_OFF + g * CHUNK_BYTES;
 #pragma unroll
-        for (int uu = 0; uu < 4; ++uu) {
-          const int unit = (jc & 1) * 4 + uu;
-          st_swizzled_unit(ptb, r, unit, make_uint4(pp[4 * uu], pp[4 * uu + 1], pp[4 * uu + 2], pp[4 * uu + 3]));
-          st_swizzled_unit(dsb, r, unit, make_uint4(dd[4 * uu], dd[4 * uu + 1], dd[4 * uu + 2], dd[4 * uu + 3]));
-        }
+        for (int uu = 0; uu < 4; ++uu)
+          st_swizzled_unit(dsb, r, 4 * jc + uu, make_uint4(dd[4 * uu], dd[4 * uu + 1], dd[4 * uu + 2], dd[4 * uu + 3]));
       }
+      tmem_wait_st();
       tc_fence_before();
       fence_proxy_async_smem();
       mbar_arrive(ds_ready);
@@ -308,12 +336,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int qi = qt * TILE + r;
       float* dst = p.dqacc + (size_t)h * HD * p.Npad + qi;
 #pragma unroll 1
-      for (int jc = 0; jc < HD / 32; ++jc) {
+      for (int jc = 0; jc < HD / 64; ++jc) {
+        const int c0 = (HD / 2) * g + 32 * jc;
         uint32_t qr[32];
-        tmem_load32(lane_base + C::DQ_COL + jc * 32, qr);
+        tmem_load32(tmem + lane_off + C::B_COL + c0, qr);
         if (qi < p.N) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) atomicAdd(dst + (size_t)(jc * 32 + c) * p.Npad, __uint_as_float(qr[c]));
+          for (int c = 0; c < 32; ++c) atomicAdd(dst + (size_t)(c0 + c) * p.Npad, __uint_as_float(qr[c]));
         }
       }
       tc_fence_before();
@@ -321,14 +350,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     if (ok && mbar_wait_warp(dkdv_done, 0, wc)) {
       tc_fence_after();
-      // dV row j
+      // dV row j, columns [HD/2 g, HD/2 (g+1))
       __nv_bfloat16* dvrow = p.dv + ((size_t)j * p.Hkv + kvh) * HD;
 #pragma unroll 1
-      for (int jc = 0; jc < HD / 32; ++jc) {
+      for (int jc = 0; jc < HD / 64; ++jc) {
+        const int c0 = (HD / 2) * g + 32 * jc;
         uint32_t a[32];
-        tmem_load32(lane_base + C::DV_COL + jc * 32, a);
+        tmem_load32(tmem + lane_off + C::DV_COL + c0, a);
         if (j < p.N) {
-          uint4* d4 = reinterpret_cast<uint4*>(dvrow + jc * 32);
+          uint4* d4 = reinterpret_cast<uint4*>(dvrow + c0);
 #pragma unroll
           for (int v = 0; v < 4; ++v)
             d4[v] = make_uint4(pack_bf16(__uint_as_float(a[8 * v + 0]), __uint_as_float(a[8 * v + 1])),
@@ -337,21 +367,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                pack_bf16(__uint_as_float(a[8 * v + 6]), __uint_as_float(a[8 * v + 7])));
         }
       }
-      // dK row j with the inverse RoPE rotation: columns c and c + HD/2 pair up
+      // dK row j with the inverse RoPE rotation: group g takes the pairs (c, c + HD/2),
+      // c in [HD/4 g, HD/4 (g+1))
       __nv_bfloat16* dkrow = p.dk + ((size_t)j * p.Hkv + kvh) * HD;
       const float posf = (j < p.N) ? static_cast<float>(p.pos[j]) : 0.f;
 #pragma unroll 1
       for (int jc = 0; jc < HD / 64; ++jc) {
-        uint32_t a[32], b[32];
-        tmem_load32(lane_base + C::DK_COL + jc * 32, a);
-        tmem_load32(lane_base + C::DK_COL + HD / 2 + jc * 32, b);
-        float lo[32], hi[32];
+        const int c0 = (HD / 4) * g + 16 * jc;
+        uint32_t a[16], b[16];
+        tmem_load16(tmem + lane_off + C::DK_COL + c0, a);
+        tmem_load16(tmem + lane_off + C::DK_COL + HD / 2 + c0, b);
+        float lo[16], hi[16];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
+        for (int c = 0; c < 16; ++c) {
           const float g1 = __uint_as_float(a[c]), g2 = __uint_as_float(b[c]);
           if (p.rope_theta > 0.f) {
             float sv, cv;
-            sincosf(posf * rope_inv_freq(jc * 32 + c, HD, p.rope_theta), &sv, &cv);
+            sincosf(posf * rope_inv_freq(c0 + c, HD, p.rope_theta), &sv, &cv);
             lo[c] = g1 * cv + g2 * sv;
             hi[c] = g2 * cv - g1 * sv;
           } else {
@@ -360,10 +392,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
         }
         if (j < p.N) {
-          uint4* d4 = reinterpret_cast<uint4*>(dkrow + jc * 32);
-          uint4* e4 = reinterpret_cast<uint4*>(dkrow + HD / 2 + jc * 32);
+          uint4* d4 = reinterpret_cast<uint4*>(dkrow + c0);
+          uint4* e4 = reinterpret_cast<uint4*>(dkrow + HD / 2 + c0);
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
+          for (int v = 0; v < 2; ++v) {
             d4[v] = make_uint4(pack_bf16(lo[8 * v], lo[8 * v + 1]), pack_bf16(lo[8 * v + 2], lo[8 * v + 3]),
                                pack_bf16(lo[8 * v + 4], lo[8 * v + 5]), pack_bf16(lo[8 * v + 6], lo[8 * v + 7]));
             e4[v] = make_uint4(pack_bf16(hi[8 * v], hi[8 * v + 1]), pack_bf16(hi[8 * v + 2], hi[8 * v + 3]),
@@ -384,10 +416,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 // ------------------------------------------------------------------------------------------
 // dQ = R(pos)^T dQacc: one block per 32 tokens, all heads; angles computed once per token.
+// Per head: the [d][32] fp32 slab is read with 16-byte loads (one 128-byte line per row of
+// 32 tokens), transposed through shared memory, rotated, and written as 16-byte bf16 stores.
 template <int HD>
 __global__ void __launch_bounds__(256) k_dq_finalize(const float* __restrict__ dqacc, const int32_t* __restrict__ pos,
                                                      __nv_bfloat16* dq, int N, int Npad, int Hq, float theta) {
-  constexpr int TT = 32, HALF = HD / 2;
+  constexpr int TT = 32, HALF = HD / 2, G = HALF / 8;   // G groups of 8 columns per half row
   __shared__ float s_cos[TT][HALF], s_sin[TT][HALF];
   __shared__ float tile[HD][TT + 1];
   const int i0 = blockIdx.x * TT;
@@ -399,23 +433,39 @@ __global__ void __launch_bounds__(256) k_dq_finalize(const float* __restrict__ d
     s_cos[t][c] = cv;
     s_sin[t][c] = sv;
   }
+  const int t_out = threadIdx.x / G, g_out = threadIdx.x % G;
   for (int h = 0; h < Hq; ++h) {
     __syncthreads();
     const float* src = dqacc + (size_t)h * HD * Npad + i0;
-    for (int e = threadIdx.x; e < HD * TT; e += blockDim.x) {
-      const int c = e / TT, t = e % TT;
-      tile[c][t] = src[(size_t)c * Npad + t];
+    for (int e = threadIdx.x; e < HD * (TT / 4); e += blockDim.x) {
+      const int c = e / (TT / 4), t4 = e % (TT / 4);
+      const float4 v = *reinterpret_cast<const float4*>(src + (size_t)c * Npad + 4 * t4);
+      tile[c][4 * t4 + 0] = v.x;
+      tile[c][4 * t4 + 1] = v.y;
+      tile[c][4 * t4 + 2] = v.z;
+      tile[c][4 * t4 + 3] = v.w;
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < TT * HALF; e += blockDim.x) {
-      const int t = e / HALF, c = e % HALF;
-      const int i = i0 + t;
-      if (i >= N) continue;
-      const float g1 = tile[c][t], g2 = tile[c + HALF][t];
-      const float cv = s_cos[t][c], sv = s_sin[t][c];
+    const int i = i0 + t_out;
+    if (t_out < TT && i < N) {
+      uint32_t lo[4], hi[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float a[2], b[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int c = 8 * g_out + 2 * e + k;
+          const float g1 = tile[c][t_out], g2 = tile[c + HALF][t_out];
+          const float cv = s_cos[t_out][c], sv = s_sin[t_out][c];
+          a[k] = g1 * cv + g2 * sv;
+          b[k] = g2 * cv - g1 * sv;
+        }
+        lo[e] = pack_bf16(a[0], a[1]);
+        hi[e] = pack_bf16(b[0], b[1]);
+      }
       __nv_bfloat16* row = dq + ((size_t)i * Hq + h) * HD;
-      row[c] = __float2bfloat16_rn(g1 * cv + g2 * sv);
-      row[c + HALF] = __float2bfloat16_rn(g2 * cv - g1 * sv);
+      *reinterpret_cast<uint4*>(row + 8 * g_out) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      *reinterpret_cast<uint4*>(row + HALF + 8 * g_out) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
     }
   }
 }
@@ -452,7 +502,7 @@ int launch_bwd(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k, 
               reinterpret_cast<__nv_bfloat16*>(dv), status, N, T, Npad, Hq, Hkv, Hq / Hkv, scale,
               scale * 1.4426950408889634f, theta, wait_limit_ns()};
   record_timing_event(1, s);
-  k_bwd_dkdv<HD><<<T * Hkv, kBwdThreads, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, P);
+  k_bwd_dkdv<HD><<<T * Hkv, C::THREADS, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, P);
   record_timing_event(2, s);
   k_dq_finalize<HD><<<(N + 31) / 32, 256, 0, s>>>(dqacc, plan->pos, reinterpret_cast<__nv_bfloat16*>(dq), N, Npad,
                                                   Hq, theta);

@@ -25,6 +25,8 @@
 namespace ta {
 namespace {
 
+constexpr int kMaxList = 1024;      // row lists up to this length are staged in shared memory
+
 template <int HD, int NH>
 struct FwdCfg {
   static constexpr int NCH = HD / 64;                 // 64-column (128-byte) chunks per row
@@ -34,7 +36,9 @@ struct FwdCfg {
   static constexpr int V_OFF = K_OFF + NS * NCH * CHUNK_BYTES;
   static constexpr int KIN_OFF = V_OFF + NS * NCH * CHUNK_BYTES;
   static constexpr int KOUT_OFF = KIN_OFF + NS * TILE * 4;
-  static constexpr int BAR_OFF = KOUT_OFF + NS * TILE * 4;
+  static constexpr int LIST_OFF = KOUT_OFF + NS * TILE * 4;    // int32 key tiles of the row
+  static constexpr int LCLS_OFF = LIST_OFF + kMaxList * 4;     // uint8 their tile classes
+  static constexpr int BAR_OFF = LCLS_OFF + kMaxList;
   static constexpr int NBAR = 1 + 2 * NS + 3 * NH + 1;  // q, kv full/empty, s/p/o per head, drain
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int SMEM = MISC_OFF + 16;
@@ -104,6 +108,17 @@ __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
   const int kvh = h0 / p.grp;
   const int rp0 = p.row_ptr[qt];
   const int cnt = p.row_ptr[qt + 1] - rp0;
+  int32_t* list_s = reinterpret_cast<int32_t*>(sm + C::LIST_OFF);
+  uint8_t* lcls_s = sm + C::LCLS_OFF;
+  for (int i = threadIdx.x; i < cnt && i < kMaxList; i += blockDim.x) {   // the row's key tiles, staged once
+    const int kt = p.row_idx[rp0 + i];
+    list_s[i] = kt;
+    lcls_s[i] = p.tile_class[(size_t)qt * p.T + kt];
+  }
+  auto row_tile = [&](int n, int& kt, int& cls) {
+    if (n < kMaxList) { kt = list_s[n]; cls = lcls_s[n]; }
+    else { kt = p.row_idx[rp0 + n]; cls = p.tile_class[(size_t)qt * p.T + kt]; }
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -137,7 +152,8 @@ __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
       for (int n = 0; n < cnt; ++n) {
         const int s = n % C::NS;
         if (n >= C::NS && !mbar_wait(&kv_empty[s], ((n / C::NS) - 1) & 1, wc)) break;
-        const int kt = p.row_idx[rp0 + n];
+        int kt, cls;
+        row_tile(n, kt, cls);
         mbar_expect_tx(&kv_full[s], C::KV_TX);
         uint8_t* kb = sm + C::K_OFF + s * C::NCH * CHUNK_BYTES;
         uint8_t* vb = sm + C::V_OFF + s * C::NCH * CHUNK_BYTES;
@@ -224,8 +240,8 @@ __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
     bool ok = true;
     for (int n = 0; n < cnt; ++n) {
       const int s = n % C::NS;
-      const int kt = p.row_idx[rp0 + n];
-      const uint8_t cls = p.tile_class[(size_t)qt * p.T + kt];
+      int kt, cls;
+      row_tile(n, kt, cls);
       if (!mbar_wait_warp(&s_full[wg], n & 1, wc)) { ok = false; break; }
       tc_fence_after();
       uint32_t sv[TILE];
