@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
   const int kvh = u % p.Hkv;
   const int cp0 = p.col_ptr[kt];
   const int ccnt = p.col_ptr[kt + 1] - cp0;
-  const int total = ccnt * p.grp;               // steps: q head (outer) x query tile (inner, descending)
+  const int total = ccnt * p.grp;               // steps: query tile (outer, descending) x q head (inner)
 
   // the column's query tiles and their classes, staged once
   for (int i = threadIdx.x; i < ccnt && i < kMaxList; i += blockDim.x) {
@@ -155,11 +155,12 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
     list_s[i] = qt;
     lcls_s[i] = p.tile_class[(size_t)qt * p.T + kt];
   }
-  // step n -> (q head, query tile, class); tiles are taken from the end of the column so that
-  // the CTAs running at one time work on the same query tiles (their dQ lines stay in L2)
+  // step n -> (q head, query tile, class).  Query tiles are walked from the end of the column
+  // with the group's q heads innermost, so CTAs running at the same time (whatever their key
+  // tile) reach the same (query tile, head) pairs together and their dQ lines stay in L2.
   auto step_tile = [&](int n, int& h, int& qt, int& cls) {
-    const int i = ccnt - 1 - n % ccnt;
-    h = kvh * p.grp + n / ccnt;
+    const int i = ccnt - 1 - n / p.grp;
+    h = kvh * p.grp + n % p.grp;
     if (i < kMaxList) { qt = list_s[i]; cls = lcls_s[i]; }
     else { qt = p.col_idx[cp0 + i]; cls = p.tile_class[(size_t)qt * p.T + kt]; }
   };
@@ -281,7 +282,9 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const int j = kt * TILE + r;
     const int kin = p.tok_in[j], kout = p.tok_out[j];
-    const float nl2e = -1.4426950408889634f;
+    const uint64_t nl2e2 = f2_pack(-1.4426950408889634f, -1.4426950408889634f);
+    const uint64_t sl2x2 = f2_pack(p.scale_log2, p.scale_log2);
+    const uint64_t sc2 = f2_pack(p.scale, p.scale), nsc2 = f2_pack(-p.scale, -p.scale);
     bool ok = true;
     for (int n = 0; n < total; ++n) {
       int h, qt, cls;
@@ -300,25 +303,32 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
         uint32_t pp[16], dd[16];
 #pragma unroll
         for (int c = 0; c < 32; c += 4) {
+          // per column: -LSE log2e and -delta scale, in pairs
           const float4 l4 = *reinterpret_cast<const float4*>(lse_s + c0 + c);
           const float4 d4 = *reinterpret_cast<const float4*>(dlt_s + c0 + c);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dl[4] = {d4.x, d4.y, d4.z, d4.w};
-          float pv[4], dsv[4];
+          const uint64_t nl01 = f2_mul(f2_pack(l4.x, l4.y), nl2e2), nl23 = f2_mul(f2_pack(l4.z, l4.w), nl2e2);
+          const uint64_t nd01 = f2_mul(f2_pack(d4.x, d4.y), nsc2), nd23 = f2_mul(f2_pack(d4.z, d4.w), nsc2);
+          float x0, x1, x2, x3;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2, nl01), x0, x1);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])), sl2x2, nl23), x2, x3);
+          float pv[4] = {ex2_approx(x0), ex2_approx(x1), ex2_approx(x2), ex2_approx(x3)};
+          if (cls == 1) {
+            const int4 qi4 = *reinterpret_cast<const int4*>(qin_s + c0 + c);
+            const int qv[4] = {qi4.x, qi4.y, qi4.z, qi4.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float pe = ex2_approx(fmaf(__uint_as_float(sr[c + e]), p.scale_log2, lv[e] * nl2e));
-            if (cls == 1) {
-              const int i = c0 + c + e;
-              const int qi_in = qin_s[i];
-              pe = ((i >= jrel) && (kin <= qi_in) && (qi_in <= kout)) ? pe : 0.f;
-            }
-            pv[e] = pe;
-            dsv[e] = pe * (__uint_as_float(dr[c + e]) - dl[e]) * p.scale;
+            for (int e = 0; e < 4; ++e)
+              pv[e] = ((c0 + c + e >= jrel) && (kin <= qv[e]) && (qv[e] <= kout)) ? pv[e] : 0.f;
           }
+          // dS = P (dP - delta) scale = P (dP scale - delta scale)
+          const uint64_t t01 = f2_fma(f2_pack(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), sc2, nd01);
+          const uint64_t t23 = f2_fma(f2_pack(__uint_as_float(dr[c + 2]), __uint_as_float(dr[c + 3])), sc2, nd23);
+          float d0, d1, d2, d3;
+          f2_unpack(f2_mul(f2_pack(pv[0], pv[1]), t01), d0, d1);
+          f2_unpack(f2_mul(f2_pack(pv[2], pv[3]), t23), d2, d3);
           pp[c >> 1] = pack_bf16(pv[0], pv[1]);
           pp[(c >> 1) + 1] = pack_bf16(pv[2], pv[3]);
-          dd[c >> 1] = pack_bf16(dsv[0], dsv[1]);
-          dd[(c >> 1) + 1] = pack_bf16(dsv[2], dsv[3]);
+          dd[c >> 1] = pack_bf16(d0, d1);
+          dd[(c >> 1) + 1] = pack_bf16(d2, d3);
         }
         // P^T for these 32 queries: 16 packed columns inside this group's own S^T columns
         tmem_store16(tmem + lane_off + C::A_COL + 64 * g + 16 * jc, pp);

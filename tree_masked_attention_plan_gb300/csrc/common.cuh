@@ -149,6 +149,22 @@ DEVI void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
 // make this thread's generic-proxy shared-memory writes visible to the async proxy (UMMA)
 DEVI void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// element-wise atomic add of a shared-memory box into global memory through a 2-D tensor map
+// (the box layout in shared memory is row-major, unswizzled); completion via bulk groups
+DEVI void tma_reduce_add_2d(const CUtensorMap* m, const void* src, int c0, int c1) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(c0), "r"(c1), "r"(smem_u32(src))
+      : "memory");
+}
+DEVI void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// wait until the shared-memory sources of every committed bulk group have been read
+DEVI void bulk_wait_group_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// wait until every committed bulk group has completed (its global writes performed)
+DEVI void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+DEVI void named_bar_sync(int id, int count) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory"); }
+
 // ------------------------------------------------------------------------------------------
 // tcgen05
 DEVI void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {   // whole warp
@@ -293,6 +309,7 @@ namespace ta {
 int check_device();                                  // TREE_OK or TREE_ERR_ARCH / TREE_ERR_CUDA
 int record_cuda(cudaError_t e);                      // TREE_OK or TREE_ERR_CUDA (message kept)
 int make_tmap_bf16_3d(CUtensorMap* m, const void* base, int d, int heads, int rows);
+int make_tmap_f32_2d(CUtensorMap* m, const void* base, int inner, int rows, int box_inner, int box_rows);
 uint64_t wait_limit_ns();
 int plan_ok(const tree_plan_t* p);
 void record_timing_event(int i, cudaStream_t s);     // no-op unless events are registered
