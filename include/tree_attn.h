@@ -96,7 +96,8 @@ typedef struct {
   int32_t* col_ptr;       /* [T+1] CSR over key tiles */
   int32_t* col_idx;       /* [max_nnz] non-empty qt of each kt, ascending */
   int32_t* row_order;     /* [T] query tiles by descending row count (ties: ascending) */
-  int32_t* col_order;     /* [T] key tiles by descending column count (ties: ascending) */
+  int32_t* col_order;     /* [T] key tiles by descending last query tile of their column,
+                             then descending column count (ties: ascending index) */
   int32_t* tile_hi_min;   /* [T] min of hi over the key tile's real tokens */
   int32_t* tile_hi_max;   /* [T] max of hi over the key tile's real tokens */
   int32_t* counts;        /* [4] nnz, n_full, n_partial, reserved (0) */
@@ -153,7 +154,7 @@ int tree_attn_fwd(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* 
                   float* lse, int32_t* status_dev, tree_stream_t stream);
 
 /* Bytes of device workspace tree_attn_bwd needs: delta [Hq][N_pad] fp32 followed by the
- * fp32 dQ accumulator [Hq][d][N_pad]. */
+ * fp32 dQ accumulator (Hq * d * N_pad floats, one block per head and query tile). */
 size_t tree_attn_bwd_workspace(const tree_plan_t* plan, int Hq, int d);
 
 /* Backward of tree_attn_fwd (section 6.2: gradients of shared ancestors add up).

@@ -237,7 +237,8 @@ def tile_classes(parent, node_len, tile: int = TILE, _plan=None):
     rcount = np.diff(row_ptr)
     ccount = np.diff(col_ptr)
     row_order = np.array(sorted(range(T), key=lambda q: (-rcount[q], q)), dtype=np.int64)
-    col_order = np.array(sorted(range(T), key=lambda k: (-ccount[k], k)), dtype=np.int64)
+    last_q = [max((q for q in range(T) if cls[q, k] != 0), default=-1) for k in range(T)]
+    col_order = np.array(sorted(range(T), key=lambda k: (-last_q[k], -ccount[k], k)), dtype=np.int64)
     return dict(n_tiles=T, tile_pairs=cnt, tile_class=cls.reshape(-1), row_ptr=row_ptr,
                 row_idx=np.array(row_idx, dtype=np.int64), col_ptr=col_ptr,
                 col_idx=np.array(col_idx, dtype=np.int64), row_order=row_order,

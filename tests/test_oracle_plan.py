@@ -226,8 +226,10 @@ def test_tile_classes_pairwise(tile, seed):
         assert ci[cp[k]:cp[k + 1]].tolist() == [q for q in range(T) if cls[q, k]]
     rc = np.diff(rp)[p["row_order"]]
     assert sorted(p["row_order"].tolist()) == list(range(T)) and np.all(np.diff(rc) <= 0)
-    cc = np.diff(cp)[p["col_order"]]
-    assert sorted(p["col_order"].tolist()) == list(range(T)) and np.all(np.diff(cc) <= 0)
+    # columns: by descending last non-empty query tile, then descending count, then index
+    last = [max(q for q in range(T) if cls[q, k]) for k in range(T)]
+    key = [(-last[k], -(cp[k + 1] - cp[k]), k) for k in p["col_order"]]
+    assert sorted(p["col_order"].tolist()) == list(range(T)) and key == sorted(key)
     assert p["nnz"] == int((cls != 0).sum()) == p["n_full"] + p["n_partial"]
 
 

@@ -14,6 +14,8 @@
 //                                            accumulator with coalesced red.global.add.
 //                  dK gets the inverse RoPE rotation in the epilogue.
 //   k_dq_finalize  dQ = R(pos)^T dQacc, fp32 -> bf16, token-major.
+// The fp32 dQ accumulator keeps each (head, query tile) block contiguous ([d][128] per block),
+// so the reductions of the CTAs working on one query tile touch one compact region of L2.
 #include <algorithm>
 #include <cmath>
 
@@ -63,7 +65,7 @@ struct BwdParams {
   const uint8_t* tile_class;
   const float* lse;          // [Hq][Npad]
   const float* dlt;          // [Hq][Npad]
-  float* dqacc;              // [Hq][HD][Npad]
+  float* dqacc;              // [Hq][T][HD][128]: one contiguous 64 KiB block per (head, query tile)
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int32_t* status;
@@ -344,7 +346,7 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
       if (!mbar_wait_warp(dq_full, n & 1, wc)) { ok = false; break; }
       tc_fence_after();
       const int qi = qt * TILE + r;
-      float* dst = p.dqacc + (size_t)h * HD * p.Npad + qi;
+      float* dst = p.dqacc + ((size_t)h * p.T + qt) * HD * TILE + r;
 #pragma unroll 1
       for (int jc = 0; jc < HD / 64; ++jc) {
         const int c0 = (HD / 2) * g + 32 * jc;
@@ -352,7 +354,7 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
         tmem_load32(tmem + lane_off + C::B_COL + c0, qr);
         if (qi < p.N) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) atomicAdd(dst + (size_t)(c0 + c) * p.Npad, __uint_as_float(qr[c]));
+          for (int c = 0; c < 32; ++c) atomicAdd(dst + (c0 + c) * TILE, __uint_as_float(qr[c]));
         }
       }
       tc_fence_before();
@@ -430,7 +432,7 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
 // 32 tokens), transposed through shared memory, rotated, and written as 16-byte bf16 stores.
 template <int HD>
 __global__ void __launch_bounds__(256) k_dq_finalize(const float* __restrict__ dqacc, const int32_t* __restrict__ pos,
-                                                     __nv_bfloat16* dq, int N, int Npad, int Hq, float theta) {
+                                                     __nv_bfloat16* dq, int N, int T, int Hq, float theta) {
   constexpr int TT = 32, HALF = HD / 2, G = HALF / 8;   // G groups of 8 columns per half row
   __shared__ float s_cos[TT][HALF], s_sin[TT][HALF];
   __shared__ float tile[HD][TT + 1];
@@ -446,10 +448,10 @@ __global__ void __launch_bounds__(256) k_dq_finalize(const float* __restrict__ d
   const int t_out = threadIdx.x / G, g_out = threadIdx.x % G;
   for (int h = 0; h < Hq; ++h) {
     __syncthreads();
-    const float* src = dqacc + (size_t)h * HD * Npad + i0;
+    const float* src = dqacc + ((size_t)h * T + i0 / TILE) * HD * TILE + i0 % TILE;
     for (int e = threadIdx.x; e < HD * (TT / 4); e += blockDim.x) {
       const int c = e / (TT / 4), t4 = e % (TT / 4);
-      const float4 v = *reinterpret_cast<const float4*>(src + (size_t)c * Npad + 4 * t4);
+      const float4 v = *reinterpret_cast<const float4*>(src + (size_t)c * TILE + 4 * t4);
       tile[c][4 * t4 + 0] = v.x;
       tile[c][4 * t4 + 1] = v.y;
       tile[c][4 * t4 + 2] = v.z;
@@ -514,8 +516,8 @@ int launch_bwd(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k, 
   record_timing_event(1, s);
   k_bwd_dkdv<HD><<<T * Hkv, C::THREADS, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, P);
   record_timing_event(2, s);
-  k_dq_finalize<HD><<<(N + 31) / 32, 256, 0, s>>>(dqacc, plan->pos, reinterpret_cast<__nv_bfloat16*>(dq), N, Npad,
-                                                  Hq, theta);
+  k_dq_finalize<HD><<<(N + 31) / 32, 256, 0, s>>>(dqacc, plan->pos, reinterpret_cast<__nv_bfloat16*>(dq), N, T, Hq,
+                                                  theta);
   record_timing_event(3, s);
   return record_cuda(cudaGetLastError());
 }

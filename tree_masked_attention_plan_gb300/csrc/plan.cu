@@ -236,18 +236,20 @@ __global__ void k_tile_cols(int N, int T, const int32_t* hmin, const int32_t* hm
 
 // single block: counts -> exclusive prefix sums (in place), and heaviest-first orders
 __global__ void k_tile_scan_order(int T, int32_t* row_ptr, int32_t* col_ptr, int32_t* row_order,
-                                  int32_t* col_order) {
+                                  int32_t* col_order, const int32_t* hmax) {
   __shared__ int carry[2];
   __shared__ int warp_sum[2][32];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
   // ranks first (needs the raw counts, held in ptr[1..T])
+  // rows: descending count; columns: descending last query tile (hi_max / 128), then
+  // descending count; ties by ascending index
   for (int i = threadIdx.x; i < T; i += blockDim.x) {
-    const int rc = row_ptr[i + 1], cc = col_ptr[i + 1];
+    const int rc = row_ptr[i + 1], cc = col_ptr[i + 1], cl = hmax[i] / TILE;
     int rr = 0, cr = 0;
     for (int j = 0; j < T; ++j) {
-      const int rj = row_ptr[j + 1], cj = col_ptr[j + 1];
+      const int rj = row_ptr[j + 1], cj = col_ptr[j + 1], lj = hmax[j] / TILE;
       rr += (rj > rc) || (rj == rc && j < i);
-      cr += (cj > cc) || (cj == cc && j < i);
+      cr += (lj > cl) || (lj == cl && (cj > cc || (cj == cc && j < i)));
     }
     row_order[rr] = i;
     col_order[cr] = i;
@@ -392,7 +394,7 @@ int tree_plan(const int32_t* parent, const int32_t* node_len, int32_t n_nodes, c
   k_tile_hi_range<<<T, TILE, 0, s>>>(p->hi, N, p->tile_hi_min, p->tile_hi_max);
   k_tile_rows<<<T, 256, 0, s>>>(N, T, p->tile_hi_min, p->tile_hi_max, p->tile_class, p->row_ptr + 1, p->counts);
   k_tile_cols<<<T, 256, 0, s>>>(N, T, p->tile_hi_min, p->tile_hi_max, p->col_ptr + 1);
-  k_tile_scan_order<<<1, 1024, 0, s>>>(T, p->row_ptr, p->col_ptr, p->row_order, p->col_order);
+  k_tile_scan_order<<<1, 1024, 0, s>>>(T, p->row_ptr, p->col_ptr, p->row_order, p->col_order, p->tile_hi_max);
   k_tile_fill<<<dim3(T, 2), 256, 0, s>>>(T, p->tile_class, p->row_ptr, p->row_idx, p->col_ptr, p->col_idx);
   return record_cuda(cudaGetLastError());
 }
