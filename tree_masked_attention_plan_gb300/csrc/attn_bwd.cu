@@ -44,7 +44,12 @@ struct BwdCfg {
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int SMEM = MISC_OFF + 16;
   static constexpr int SMEM_ALLOC = SMEM + 1024;
-  static constexpr int THREADS = 64 + 256;                      // producer, MMA, 8 elementwise warps
+  // 16 warps = 4 warpgroups: [producer, MMA, 2 idle] [4 dQ drain] [4 + 4 elementwise]
+  static constexpr int THREADS = 512;
+  static constexpr int LAUNCH_REGS = 128;                      // 512 x 128 = the whole register file
+  static constexpr int REGS_CTRL = 48, REGS_DRAIN = 144, REGS_EW = 160;
+  static_assert(128 * REGS_CTRL + 128 * REGS_DRAIN + 256 * REGS_EW <= THREADS * LAUNCH_REGS,
+                "register re-balancing must fit the launch allocation");
   static constexpr uint32_t TMEM_COLS = 512;
   // TMEM columns: S^T in A (P^T packed bf16 over it, query half g at 64 g), dP^T and dQ in B
   static constexpr uint32_t A_COL = 0, B_COL = 128, DV_COL = 256, DK_COL = 256 + HD;
@@ -174,7 +179,7 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
     mbar_init(sdp_full, 1);
     mbar_init(ds_ready, 256);
     mbar_init(dq_full, 1);
-    mbar_init(dq_free, 256);
+    mbar_init(dq_free, 128);
     mbar_init(dkdv_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -190,6 +195,8 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{abort_flag, p.status, p.wait_ns};
 
+  if (warp < 4) {
+    regs_dec<C::REGS_CTRL>();
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
@@ -274,11 +281,42 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
       umma_commit(drain);
       mbar_wait_drain_b(drain, 0, p.wait_ns);
     }
+  }
+  } else if (warp < 8) {
+    regs_inc<C::REGS_DRAIN>();
+    // ---------------------------------------------------------------- dQ drain warpgroup
+    // Thread r copies dQ(n) row r (all HD columns) out of TMEM, frees the columns for dP(n+1),
+    // then adds the row into the fp32 accumulator with coalesced red.global.add (a warp
+    // instruction covers one column of 32 consecutive query rows) while the next step runs.
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    for (int n = 0; n < total; ++n) {
+      int h, qt, cls;
+      step_tile(n, h, qt, cls);
+      if (!mbar_wait_warp(dq_full, n & 1, wc)) break;
+      tc_fence_after();
+      uint32_t qv[HD];
+#pragma unroll
+      for (int jc = 0; jc < HD / 32; ++jc)
+        tmem_ld32(tmem + lane_off + C::B_COL + 32 * jc, *reinterpret_cast<uint32_t(*)[32]>(qv + 32 * jc));
+#pragma unroll
+      for (int jc = 0; jc < HD / 32; ++jc) tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(qv + 32 * jc));
+      tc_fence_before();
+      mbar_arrive(dq_free);
+      const int qi = qt * TILE + r;
+      if (qi < p.N) {
+        float* dst = p.dqacc + ((size_t)h * p.T + qt) * HD * TILE + r;
+#pragma unroll
+        for (int c = 0; c < HD; ++c) atomicAdd(dst + c * TILE, __uint_as_float(qv[c]));
+      }
+    }
   } else {
+    regs_inc<C::REGS_EW>();
     // ---------------------------------------------------------------- elementwise warps
     // Two warpgroups share the 128 TMEM lanes: group g takes query columns [64 g, 64 g + 64)
-    // of S^T / dP^T, and output columns [HD/2 g, HD/2 (g+1)) of dQ and dV.
-    const int g = (warp - 2) >> 2;
+    // of S^T / dP^T, and output columns [HD/2 g, HD/2 (g+1)) of dV, pairs of dK.
+    const int g = (warp - 8) >> 2;
     const int wq = warp & 3;
     const int r = wq * 32 + lane;                 // key row (S^T, dP^T, dK, dV) or query row (dQ)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
@@ -343,22 +381,6 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
       tc_fence_before();
       fence_proxy_async_smem();
       mbar_arrive(ds_ready);
-      if (!mbar_wait_warp(dq_full, n & 1, wc)) { ok = false; break; }
-      tc_fence_after();
-      const int qi = qt * TILE + r;
-      float* dst = p.dqacc + ((size_t)h * p.T + qt) * HD * TILE + r;
-#pragma unroll 1
-      for (int jc = 0; jc < HD / 64; ++jc) {
-        const int c0 = (HD / 2) * g + 32 * jc;
-        uint32_t qr[32];
-        tmem_load32(tmem + lane_off + C::B_COL + c0, qr);
-        if (qi < p.N) {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) atomicAdd(dst + (c0 + c) * TILE, __uint_as_float(qr[c]));
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(dq_free);
     }
     if (ok && mbar_wait_warp(dkdv_done, 0, wc)) {
       tc_fence_after();
@@ -500,6 +522,17 @@ int launch_bwd(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k, 
   if (rc) return rc;
   rc = record_cuda(cudaFuncSetAttribute(k_bwd_dkdv<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC));
   if (rc) return rc;
+  {
+    // setmaxnreg.inc waits for registers released by other warpgroups of the CTA: the
+    // re-balancing only adds up if the kernel launches with exactly LAUNCH_REGS per thread.
+    cudaFuncAttributes fa;
+    rc = record_cuda(cudaFuncGetAttributes(&fa, k_bwd_dkdv<HD>));
+    if (rc) return rc;
+    if (fa.numRegs != C::LAUNCH_REGS) {
+      record_cuda(cudaErrorInvalidConfiguration);
+      return TREE_ERR_CUDA;
+    }
+  }
   record_timing_event(0, s);
   {
     const size_t threads = (size_t)Npad * Hq * (HD / 8);

@@ -165,6 +165,12 @@ DEVI void bulk_wait_group_read0() { asm volatile("cp.async.bulk.wait_group.read 
 DEVI void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 DEVI void named_bar_sync(int id, int count) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory"); }
 
+// Per-warpgroup register re-balancing (all four warps of a warpgroup execute it together).
+template <int N>
+DEVI void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
+template <int N>
+DEVI void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+
 // ------------------------------------------------------------------------------------------
 // tcgen05
 DEVI void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {   // whole warp
