@@ -31,8 +31,8 @@ struct BwdCfg {
   static constexpr int NCH = HD / 64;
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = K_OFF + NCH * CHUNK_BYTES;
-  static constexpr int Q_OFF = V_OFF + NCH * CHUNK_BYTES;
-  static constexpr int DO_OFF = Q_OFF + NCH * CHUNK_BYTES;
+  static constexpr int Q_OFF = V_OFF + NCH * CHUNK_BYTES;     // two stages
+  static constexpr int DO_OFF = Q_OFF + 2 * NCH * CHUNK_BYTES;
   static constexpr int DST_OFF = DO_OFF + NCH * CHUNK_BYTES;
   static constexpr int LSE_OFF = DST_OFF + 2 * CHUNK_BYTES;
   static constexpr int DLT_OFF = LSE_OFF + TILE * 4;
@@ -40,7 +40,7 @@ struct BwdCfg {
   static constexpr int LIST_OFF = QIN_OFF + TILE * 4;           // int32 query tiles of the column
   static constexpr int LCLS_OFF = LIST_OFF + kMaxList * 4;     // uint8 their tile classes
   static constexpr int BAR_OFF = LCLS_OFF + kMaxList;
-  static constexpr int NBAR = 9;
+  static constexpr int NBAR = 13;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int SMEM = MISC_OFF + 16;
   static constexpr int SMEM_ALLOC = SMEM + 1024;
@@ -57,7 +57,8 @@ struct BwdCfg {
   static constexpr uint32_t IDESC_DKV = idesc_bf16(TILE, HD, 0, 1);     // P^T (TMEM) / dS^T K-major, dO/Q MN-major
   static constexpr uint32_t IDESC_DQ = idesc_bf16(TILE, HD, 1, 1);      // dS MN-major, K MN-major
   static constexpr uint32_t KV_TX = 2 * NCH * CHUNK_BYTES;
-  static constexpr uint32_t QDO_TX = 2 * NCH * CHUNK_BYTES + 3 * TILE * 4;
+  static constexpr uint32_t Q_TX = NCH * CHUNK_BYTES;
+  static constexpr uint32_t DO_TX = NCH * CHUNK_BYTES + 3 * TILE * 4;
 };
 
 struct BwdParams {
@@ -132,14 +133,16 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
   uint8_t* sm = align1024b(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::BAR_OFF);
   uint64_t* kv_full = bars + 0;
-  uint64_t* qdo_full = bars + 1;
-  uint64_t* qdo_empty = bars + 2;
+  uint64_t* do_full = bars + 1;                 // dO, LSE, delta, query dfs_in of the step
+  uint64_t* do_empty = bars + 2;
   uint64_t* sdp_full = bars + 3;
   uint64_t* ds_ready = bars + 4;
   uint64_t* dq_full = bars + 5;
   uint64_t* dq_free = bars + 6;
   uint64_t* dkdv_done = bars + 7;
   uint64_t* drain = bars + 8;
+  uint64_t* q_full = bars + 9;                  // [2] Q stages
+  uint64_t* q_empty = bars + 11;                // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::MISC_OFF);
   int* abort_flag = reinterpret_cast<int*>(sm + C::MISC_OFF + 4);
   const float* lse_s = reinterpret_cast<const float*>(sm + C::LSE_OFF);
@@ -174,8 +177,9 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    mbar_init(qdo_full, 1);
-    mbar_init(qdo_empty, 1);
+    mbar_init(do_full, 1);
+    mbar_init(do_empty, 1);
+    for (int i = 0; i < 2; ++i) { mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 1); }
     mbar_init(sdp_full, 1);
     mbar_init(ds_ready, 256);
     mbar_init(dq_full, 1);
@@ -209,36 +213,53 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
         tma_load_3d(sm + C::K_OFF + c * CHUNK_BYTES, &tmK, kv_full, c * 64, kvh, kt * TILE);
         tma_load_3d(sm + C::V_OFF + c * CHUNK_BYTES, &tmV, kv_full, c * 64, kvh, kt * TILE);
       }
-      int issued = 0;
+      auto load_q = [&](int m) {               // Q tile of step m into stage m % 2
+        int h, qt, cls;
+        step_tile(m, h, qt, cls);
+        uint64_t* bar = &q_full[m & 1];
+        mbar_expect_tx(bar, C::Q_TX);
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_3d(sm + C::Q_OFF + ((m & 1) * C::NCH + c) * CHUNK_BYTES, &tmQ, bar, c * 64, h, qt * TILE);
+      };
+      int q_issued = 0, do_issued = 0;
+      if (total > 0) { load_q(0); q_issued = 1; }
       for (int n = 0; n < total; ++n) {
         int h, qt, cls;
         step_tile(n, h, qt, cls);
-        if (n > 0 && !mbar_wait(qdo_empty, (n - 1) & 1, wc)) break;
-        mbar_expect_tx(qdo_full, C::QDO_TX);
-        for (int c = 0; c < C::NCH; ++c) {
-          tma_load_3d(sm + C::Q_OFF + c * CHUNK_BYTES, &tmQ, qdo_full, c * 64, h, qt * TILE);
-          tma_load_3d(sm + C::DO_OFF + c * CHUNK_BYTES, &tmDO, qdo_full, c * 64, h, qt * TILE);
-        }
+        // dO of step n once dV(n-1) has read the buffer
+        if (n > 0 && !mbar_wait(do_empty, (n - 1) & 1, wc)) break;
+        mbar_expect_tx(do_full, C::DO_TX);
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_3d(sm + C::DO_OFF + c * CHUNK_BYTES, &tmDO, do_full, c * 64, h, qt * TILE);
         const size_t lo = (size_t)h * p.Npad + (size_t)qt * TILE;
-        bulk_load(sm + C::LSE_OFF, p.lse + lo, TILE * 4, qdo_full);
-        bulk_load(sm + C::DLT_OFF, p.dlt + lo, TILE * 4, qdo_full);
-        bulk_load(sm + C::QIN_OFF, p.tok_in + (size_t)qt * TILE, TILE * 4, qdo_full);
-        issued = n + 1;
+        bulk_load(sm + C::LSE_OFF, p.lse + lo, TILE * 4, do_full);
+        bulk_load(sm + C::DLT_OFF, p.dlt + lo, TILE * 4, do_full);
+        bulk_load(sm + C::QIN_OFF, p.tok_in + (size_t)qt * TILE, TILE * 4, do_full);
+        do_issued = n + 1;
+        // Q of step n+1 into the other stage once dK(n-1) has read it
+        if (n + 1 < total) {
+          if (n >= 1 && !mbar_wait(&q_empty[(n + 1) & 1], (((n + 1) >> 1) - 1) & 1, wc)) break;
+          load_q(n + 1);
+          q_issued = n + 2;
+        }
       }
       if (*abort_flag) {
         mbar_wait_drain_b(kv_full, 0, p.wait_ns);
-        if (issued > 0) mbar_wait_drain_b(qdo_full, (issued - 1) & 1, p.wait_ns);
+        if (do_issued > 0) mbar_wait_drain_b(do_full, (do_issued - 1) & 1, p.wait_ns);
+        for (int m = (q_issued > 2 ? q_issued - 2 : 0); m < q_issued; ++m)
+          mbar_wait_drain_b(&q_full[m & 1], (m >> 1) & 1, p.wait_ns);
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t k_base = smem_u32(sm + C::K_OFF), v_base = smem_u32(sm + C::V_OFF);
-      const uint32_t q_base = smem_u32(sm + C::Q_OFF), do_base = smem_u32(sm + C::DO_OFF);
+      const uint32_t do_base = smem_u32(sm + C::DO_OFF);
       const uint32_t dst_base = smem_u32(sm + C::DST_OFF);
       bool ok = mbar_wait(kv_full, 0, wc);
       for (int n = 0; ok && n < total; ++n) {
-        if (!mbar_wait(qdo_full, n & 1, wc)) { ok = false; break; }
+        const uint32_t q_base = smem_u32(sm + C::Q_OFF + (n & 1) * C::NCH * CHUNK_BYTES);
+        if (!mbar_wait(&q_full[n & 1], (n >> 1) & 1, wc)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {                 // S^T = K Q^T into A (after dV(n-1) read P^T)
@@ -247,6 +268,7 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
                     C::IDESC_SDP, kk > 0 ? 1u : 0u);
         }
         if (n > 0 && !mbar_wait(dq_free, (n - 1) & 1, wc)) { ok = false; break; }
+        if (!mbar_wait(do_full, n & 1, wc)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {                 // dP^T = V dO^T into B (dQ(n-1) drained)
@@ -258,17 +280,19 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
         if (!mbar_wait(ds_ready, n & 1, wc)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < TILE / 16; ++kk) {               // dV += P^T dO (P^T from TMEM), dK += dS^T Q
+        for (int kk = 0; kk < TILE / 16; ++kk) {               // dV += P^T dO (P^T from TMEM)
           const uint32_t a_col = C::A_COL + (kk >> 2) * 64 + (kk & 3) * 8;
-          const uint32_t a_off = (kk >> 2) * CHUNK_BYTES + (kk & 3) * 32;
-          const uint32_t b_off = kk * 16 * 128;
-          const uint32_t acc = (n > 0 || kk > 0) ? 1u : 0u;
-          umma_bf16_tmem_a(tmem + C::DV_COL, tmem + a_col, sdesc_sw128(do_base + b_off, CHUNK_BYTES, 1024),
-                           C::IDESC_DKV, acc);
-          umma_bf16(tmem + C::DK_COL, sdesc_sw128(dst_base + a_off, 16, 1024),
-                    sdesc_sw128(q_base + b_off, CHUNK_BYTES, 1024), C::IDESC_DKV, acc);
+          umma_bf16_tmem_a(tmem + C::DV_COL, tmem + a_col, sdesc_sw128(do_base + kk * 16 * 128, CHUNK_BYTES, 1024),
+                           C::IDESC_DKV, (n > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(qdo_empty);                                  // Q, dO, LSE, delta free: next load starts
+        umma_commit(do_empty);                                   // dO, LSE, delta free: next load starts
+#pragma unroll
+        for (int kk = 0; kk < TILE / 16; ++kk) {               // dK += dS^T Q
+          const uint32_t a_off = (kk >> 2) * CHUNK_BYTES + (kk & 3) * 32;
+          umma_bf16(tmem + C::DK_COL, sdesc_sw128(dst_base + a_off, 16, 1024),
+                    sdesc_sw128(q_base + kk * 16 * 128, CHUNK_BYTES, 1024), C::IDESC_DKV, (n > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&q_empty[n & 1]);                            // this Q stage free
 #pragma unroll
         for (int kk = 0; kk < TILE / 16; ++kk) {               // dQ = dS K into B (keys along K)
           const uint32_t off = kk * 16 * 128;
@@ -329,7 +353,7 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
     for (int n = 0; n < total; ++n) {
       int h, qt, cls;
       step_tile(n, h, qt, cls);
-      if (!mbar_wait_warp(qdo_full, n & 1, wc) || !mbar_wait_warp(sdp_full, n & 1, wc)) { ok = false; break; }
+      if (!mbar_wait_warp(do_full, n & 1, wc) || !mbar_wait_warp(sdp_full, n & 1, wc)) { ok = false; break; }
       tc_fence_after();
       const int jrel = j - qt * TILE;             // query i is causal-visible iff i >= jrel
 #pragma unroll 1
