@@ -48,6 +48,7 @@ struct BwdCfg {
   static constexpr int THREADS = 512;
   static constexpr int LAUNCH_REGS = 128;                      // 512 x 128 = the whole register file
   static constexpr int REGS_CTRL = 48, REGS_DRAIN = 144, REGS_EW = 160;
+  static constexpr unsigned DRAIN_PACE_NS = 200;
   static_assert(128 * REGS_CTRL + 128 * REGS_DRAIN + 256 * REGS_EW <= THREADS * LAUNCH_REGS,
                 "register re-balancing must fit the launch allocation");
   static constexpr uint32_t TMEM_COLS = 512;
@@ -331,8 +332,13 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
       const int qi = qt * TILE + r;
       if (qi < p.N) {
         float* dst = p.dqacc + ((size_t)h * p.T + qt) * HD * TILE + r;
+        // paced in groups of 16 columns so the reductions spread over the next step instead of
+        // flooding the memory pipeline the elementwise warps are using at its start
 #pragma unroll
-        for (int c = 0; c < HD; ++c) atomicAdd(dst + c * TILE, __uint_as_float(qv[c]));
+        for (int c = 0; c < HD; ++c) {
+          atomicAdd(dst + c * TILE, __uint_as_float(qv[c]));
+          if ((c & 15) == 15 && c + 1 < HD) __nanosleep(C::DRAIN_PACE_NS);
+        }
       }
     }
   } else {
@@ -356,25 +362,30 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
       if (!mbar_wait_warp(do_full, n & 1, wc) || !mbar_wait_warp(sdp_full, n & 1, wc)) { ok = false; break; }
       tc_fence_after();
       const int jrel = j - qt * TILE;             // query i is causal-visible iff i >= jrel
-#pragma unroll 1
-      for (int jc = 0; jc < 2; ++jc) {
-        const int c0 = 64 * g + 32 * jc;          // first query column of this 32-wide chunk
-        uint32_t sr[32], dr[32];
-        tmem_ld32(tmem + lane_off + C::A_COL + c0, sr);
-        tmem_ld32(tmem + lane_off + C::B_COL + c0, dr);
-        tmem_wait_ld(sr);
-        tmem_wait_ld(dr);
-        uint32_t pp[16], dd[16];
+      // 4 chunks of 16 query columns; the next chunk's S^T / dP^T loads are in flight while the
+      // current chunk is computed
+      uint32_t s_cur[16], d_cur[16], s_nxt[16], d_nxt[16];
+      tmem_ld16(tmem + lane_off + C::A_COL + 64 * g, s_cur);
+      tmem_ld16(tmem + lane_off + C::B_COL + 64 * g, d_cur);
+      tmem_wait_ld16x2(s_cur, d_cur);
 #pragma unroll
-        for (int c = 0; c < 32; c += 4) {
+      for (int k = 0; k < 4; ++k) {
+        const int c0 = 64 * g + 16 * k;           // first query column of this chunk
+        if (k < 3) {
+          tmem_ld16(tmem + lane_off + C::A_COL + c0 + 16, s_nxt);
+          tmem_ld16(tmem + lane_off + C::B_COL + c0 + 16, d_nxt);
+        }
+        uint32_t pp[8], dd[8];
+#pragma unroll
+        for (int c = 0; c < 16; c += 4) {
           // per column: -LSE log2e and -delta scale, in pairs
           const float4 l4 = *reinterpret_cast<const float4*>(lse_s + c0 + c);
           const float4 d4 = *reinterpret_cast<const float4*>(dlt_s + c0 + c);
           const uint64_t nl01 = f2_mul(f2_pack(l4.x, l4.y), nl2e2), nl23 = f2_mul(f2_pack(l4.z, l4.w), nl2e2);
           const uint64_t nd01 = f2_mul(f2_pack(d4.x, d4.y), nsc2), nd23 = f2_mul(f2_pack(d4.z, d4.w), nsc2);
           float x0, x1, x2, x3;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2, nl01), x0, x1);
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])), sl2x2, nl23), x2, x3);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(s_cur[c]), __uint_as_float(s_cur[c + 1])), sl2x2, nl01), x0, x1);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(s_cur[c + 2]), __uint_as_float(s_cur[c + 3])), sl2x2, nl23), x2, x3);
           float pv[4] = {ex2_approx(x0), ex2_approx(x1), ex2_approx(x2), ex2_approx(x3)};
           if (cls == 1) {
             const int4 qi4 = *reinterpret_cast<const int4*>(qin_s + c0 + c);
@@ -384,22 +395,26 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
               pv[e] = ((c0 + c + e >= jrel) && (kin <= qv[e]) && (qv[e] <= kout)) ? pv[e] : 0.f;
           }
           // dS = P (dP - delta) scale = P (dP scale - delta scale)
-          const uint64_t t01 = f2_fma(f2_pack(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), sc2, nd01);
-          const uint64_t t23 = f2_fma(f2_pack(__uint_as_float(dr[c + 2]), __uint_as_float(dr[c + 3])), sc2, nd23);
-          float d0, d1, d2, d3;
-          f2_unpack(f2_mul(f2_pack(pv[0], pv[1]), t01), d0, d1);
-          f2_unpack(f2_mul(f2_pack(pv[2], pv[3]), t23), d2, d3);
+          const uint64_t t01 = f2_fma(f2_pack(__uint_as_float(d_cur[c]), __uint_as_float(d_cur[c + 1])), sc2, nd01);
+          const uint64_t t23 = f2_fma(f2_pack(__uint_as_float(d_cur[c + 2]), __uint_as_float(d_cur[c + 3])), sc2, nd23);
+          float e0, e1, e2, e3;
+          f2_unpack(f2_mul(f2_pack(pv[0], pv[1]), t01), e0, e1);
+          f2_unpack(f2_mul(f2_pack(pv[2], pv[3]), t23), e2, e3);
           pp[c >> 1] = pack_bf16(pv[0], pv[1]);
           pp[(c >> 1) + 1] = pack_bf16(pv[2], pv[3]);
-          dd[c >> 1] = pack_bf16(d0, d1);
-          dd[(c >> 1) + 1] = pack_bf16(d2, d3);
+          dd[c >> 1] = pack_bf16(e0, e1);
+          dd[(c >> 1) + 1] = pack_bf16(e2, e3);
         }
-        // P^T for these 32 queries: 16 packed columns inside this group's own S^T columns
-        tmem_store16(tmem + lane_off + C::A_COL + 64 * g + 16 * jc, pp);
+        // P^T for these 16 queries: 8 packed columns inside this group's already-read S^T columns
+        tmem_store8(tmem + lane_off + C::A_COL + 64 * g + 8 * k, pp);
         uint8_t* dsb = sm + C::DST_OFF + g * CHUNK_BYTES;
+        st_swizzled_unit(dsb, r, 2 * k, make_uint4(dd[0], dd[1], dd[2], dd[3]));
+        st_swizzled_unit(dsb, r, 2 * k + 1, make_uint4(dd[4], dd[5], dd[6], dd[7]));
+        if (k < 3) {
+          tmem_wait_ld16x2(s_nxt, d_nxt);
 #pragma unroll
-        for (int uu = 0; uu < 4; ++uu)
-          st_swizzled_unit(dsb, r, 4 * jc + uu, make_uint4(dd[4 * uu], dd[4 * uu + 1], dd[4 * uu + 2], dd[4 * uu + 3]));
+          for (int e = 0; e < 16; ++e) { s_cur[e] = s_nxt[e]; d_cur[e] = d_nxt[e]; }
+        }
       }
       tmem_wait_st();
       tc_fence_before();
