@@ -43,6 +43,7 @@ typedef uint16_t tree_bf16;             /* bfloat16 bit pattern */
 typedef struct CUstream_st* tree_stream_t; /* identical to cudaStream_t */
 
 #define TREE_TILE 128                   /* query and key tile edge */
+#define TREE_MAX_RUNS 16                /* node runs per tile kept in the plan's run table */
 
 enum {
   TREE_OK = 0,
@@ -100,6 +101,11 @@ typedef struct {
                              then descending column count (ties: ascending index) */
   int32_t* tile_hi_min;   /* [T] min of hi over the key tile's real tokens */
   int32_t* tile_hi_max;   /* [T] max of hi over the key tile's real tokens */
+  int32_t* tile_runs;     /* [T][TREE_MAX_RUNS][4] the tile's maximal runs of tokens of one node
+                             (padding counts as one node), in order: {start, end (exclusive),
+                             dfs_in, dfs_out} with start/end relative to the tile; only the
+                             first min(tile_nruns, TREE_MAX_RUNS) entries are written */
+  int32_t* tile_nruns;    /* [T] number of runs in the tile (may exceed TREE_MAX_RUNS) */
   int32_t* counts;        /* [4] nnz, n_full, n_partial, reserved (0) */
   int32_t n_nodes, n_tokens, n_tiles, n_paths;
 } tree_plan_t;

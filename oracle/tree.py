@@ -239,7 +239,20 @@ def tile_classes(parent, node_len, tile: int = TILE, _plan=None):
     row_order = np.array(sorted(range(T), key=lambda q: (-rcount[q], q)), dtype=np.int64)
     last_q = [max((q for q in range(T) if cls[q, k] != 0), default=-1) for k in range(T)]
     col_order = np.array(sorted(range(T), key=lambda k: (-last_q[k], -ccount[k], k)), dtype=np.int64)
-    return dict(n_tiles=T, tile_pairs=cnt, tile_class=cls.reshape(-1), row_ptr=row_ptr,
+    # runs of consecutive packed tokens that belong to one node, per tile (padding = dfs_in -1)
+    tok_in = np.full(T * tile, -1, dtype=np.int64)
+    tok_out = np.full(T * tile, -2, dtype=np.int64)
+    tok_in[:N] = p["dfs_in"][p["tok_node"]]
+    tok_out[:N] = p["dfs_out"][p["tok_node"]]
+    runs, nruns = [], []
+    for t in range(T):
+        seg = tok_in[t * tile:(t + 1) * tile]
+        st = [c for c in range(tile) if c == 0 or seg[c] != seg[c - 1]]
+        ends = st[1:] + [tile]
+        runs.append([(a, b, int(seg[a]), int(tok_out[t * tile + a])) for a, b in zip(st, ends)])
+        nruns.append(len(st))
+    return dict(n_tiles=T, tile_pairs=cnt, tile_class=cls.reshape(-1), row_ptr=row_ptr, tile_runs=runs,
+                tile_nruns=np.array(nruns, dtype=np.int64),
                 row_idx=np.array(row_idx, dtype=np.int64), col_ptr=col_ptr,
                 col_idx=np.array(col_idx, dtype=np.int64), row_order=row_order,
                 col_order=col_order, nnz=int(row_ptr[-1]), n_full=int((cls == 2).sum()),

@@ -43,6 +43,11 @@ def _check_plan(parent, node_len):
     nnz = ref["nnz"]
     assert np.array_equal(a["row_idx"][:nnz], ref["row_idx"]) and np.array_equal(a["col_idx"][:nnz], ref["col_idx"])
     assert a["counts"][:3].tolist() == [nnz, ref["n_full"], ref["n_partial"]]
+    assert np.array_equal(a["tile_nruns"], ref["tile_nruns"])
+    runs = a["tile_runs"].reshape(T, tam.MAX_RUNS, 4)
+    for t in range(T):
+        k = min(len(ref["tile_runs"][t]), tam.MAX_RUNS)
+        assert runs[t, :k].tolist() == [list(r) for r in ref["tile_runs"][t][:k]], t
 
 
 @pytest.mark.parametrize("name,tree", _trees(), ids=[t[0] for t in _trees()])

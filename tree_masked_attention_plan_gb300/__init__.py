@@ -23,6 +23,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libtreeattn.so")
 TILE = 128
+MAX_RUNS = 16
 
 TREE_OK = 0
 ERROR_NAMES = {-1: "TREE_ERR_INVALID_TREE", -2: "TREE_ERR_SHAPE", -3: "TREE_ERR_ARCH", -4: "TREE_ERR_CUDA",
@@ -51,7 +52,8 @@ class PlanInfo(ctypes.Structure):
 
 PLAN_PTR_FIELDS = ["order", "dfs_in", "dfs_out", "tok_start", "depth_off", "leaves", "dfs_tok_start", "sub_end",
                    "tok_node", "pos", "g", "tok_in", "tok_out", "hi", "w", "tile_class", "row_ptr", "row_idx",
-                   "col_ptr", "col_idx", "row_order", "col_order", "tile_hi_min", "tile_hi_max", "counts"]
+                   "col_ptr", "col_idx", "row_order", "col_order", "tile_hi_min", "tile_hi_max", "tile_runs",
+                   "tile_nruns", "counts"]
 
 
 class PlanT(ctypes.Structure):
@@ -159,7 +161,7 @@ class TreePlan:
         sizes = dict(order=n, dfs_in=n, dfs_out=n, tok_start=n, depth_off=n, leaves=n, dfs_tok_start=n,
                      sub_end=n, tok_node=Np, pos=Np, g=Np, tok_in=Np, tok_out=Np, hi=Np, w=Np,
                      tile_class=T * T, row_ptr=T + 1, row_idx=nnz, col_ptr=T + 1, col_idx=nnz, row_order=T,
-                     col_order=T, tile_hi_min=T, tile_hi_max=T, counts=4)
+                     col_order=T, tile_hi_min=T, tile_hi_max=T, tile_runs=T * MAX_RUNS * 4, tile_nruns=T, counts=4)
         base = self.buf.data_ptr()
         out = {}
         for f in PLAN_PTR_FIELDS:

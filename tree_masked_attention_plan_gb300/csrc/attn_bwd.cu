@@ -37,7 +37,8 @@ struct BwdCfg {
   static constexpr int LSE_OFF = DST_OFF + 2 * CHUNK_BYTES;
   static constexpr int DLT_OFF = LSE_OFF + TILE * 4;
   static constexpr int QIN_OFF = DLT_OFF + TILE * 4;
-  static constexpr int LIST_OFF = QIN_OFF + TILE * 4;           // int32 query tiles of the column
+  static constexpr int RUNS_OFF = QIN_OFF + TILE * 4;           // TREE_MAX_RUNS int4 node runs of the query tile
+  static constexpr int LIST_OFF = RUNS_OFF + TREE_MAX_RUNS * 16; // int32 query tiles of the column
   static constexpr int LCLS_OFF = LIST_OFF + kMaxList * 4;     // uint8 their tile classes
   static constexpr int BAR_OFF = LCLS_OFF + kMaxList;
   static constexpr int NBAR = 13;
@@ -59,7 +60,7 @@ struct BwdCfg {
   static constexpr uint32_t IDESC_DQ = idesc_bf16(TILE, HD, 1, 1);      // dS MN-major, K MN-major
   static constexpr uint32_t KV_TX = 2 * NCH * CHUNK_BYTES;
   static constexpr uint32_t Q_TX = NCH * CHUNK_BYTES;
-  static constexpr uint32_t DO_TX = NCH * CHUNK_BYTES + 3 * TILE * 4;
+  static constexpr uint32_t DO_TX = NCH * CHUNK_BYTES + 3 * TILE * 4 + TREE_MAX_RUNS * 16;
 };
 
 struct BwdParams {
@@ -69,6 +70,8 @@ struct BwdParams {
   const int32_t* tok_in;
   const int32_t* tok_out;
   const int32_t* pos;
+  const int32_t* tile_runs;
+  const int32_t* tile_nruns;
   const uint8_t* tile_class;
   const float* lse;          // [Hq][Npad]
   const float* dlt;          // [Hq][Npad]
@@ -236,6 +239,7 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
         bulk_load(sm + C::LSE_OFF, p.lse + lo, TILE * 4, do_full);
         bulk_load(sm + C::DLT_OFF, p.dlt + lo, TILE * 4, do_full);
         bulk_load(sm + C::QIN_OFF, p.tok_in + (size_t)qt * TILE, TILE * 4, do_full);
+        bulk_load(sm + C::RUNS_OFF, p.tile_runs + (size_t)qt * TREE_MAX_RUNS * 4, TREE_MAX_RUNS * 16, do_full);
         do_issued = n + 1;
         // Q of step n+1 into the other stage once dK(n-1) has read it
         if (n + 1 < total) {
@@ -362,6 +366,31 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
       if (!mbar_wait_warp(do_full, n & 1, wc) || !mbar_wait_warp(sdp_full, n & 1, wc)) { ok = false; break; }
       tc_fence_after();
       const int jrel = j - qt * TILE;             // query i is causal-visible iff i >= jrel
+      // partial tile: bits of this group's 64 query columns that key j may see, one
+      // ancestor-interval test per node run of the query tile
+      uint32_t vw0 = 0xffffffffu, vw1 = 0xffffffffu;
+      if (cls == 1) {
+        uint32_t vm[4] = {0u, 0u, 0u, 0u};
+        const int nr = p.tile_nruns[qt];
+        if (nr <= TREE_MAX_RUNS) {
+          const int4* runs = reinterpret_cast<const int4*>(sm + C::RUNS_OFF);
+          for (int k = 0; k < nr; ++k) {
+            const int4 rn = runs[k];
+            if (kin <= rn.z && rn.z <= kout) set_bits(vm, rn.x, rn.y);
+          }
+        } else {
+          for (int c4 = 0; c4 < TILE / 4; ++c4) {
+            const int4 q4 = *reinterpret_cast<const int4*>(qin_s + 4 * c4);
+            const uint32_t bits = (uint32_t)(kin <= q4.x && q4.x <= kout) | ((uint32_t)(kin <= q4.y && q4.y <= kout) << 1) |
+                                  ((uint32_t)(kin <= q4.z && q4.z <= kout) << 2) |
+                                  ((uint32_t)(kin <= q4.w && q4.w <= kout) << 3);
+            vm[c4 >> 3] |= bits << (4 * (c4 & 7));
+          }
+        }
+        set_bits_clear_below(vm, jrel);
+        vw0 = g ? vm[2] : vm[0];
+        vw1 = g ? vm[3] : vm[1];
+      }
       // 4 chunks of 16 query columns; the next chunk's S^T / dP^T loads are in flight while the
       // current chunk is computed
       uint32_t s_cur[16], d_cur[16], s_nxt[16], d_nxt[16];
@@ -388,11 +417,12 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
           f2_unpack(f2_fma(f2_pack(__uint_as_float(s_cur[c + 2]), __uint_as_float(s_cur[c + 3])), sl2x2, nl23), x2, x3);
           float pv[4] = {ex2_approx(x0), ex2_approx(x1), ex2_approx(x2), ex2_approx(x3)};
           if (cls == 1) {
-            const int4 qi4 = *reinterpret_cast<const int4*>(qin_s + c0 + c);
-            const int qv[4] = {qi4.x, qi4.y, qi4.z, qi4.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              pv[e] = ((c0 + c + e >= jrel) && (kin <= qv[e]) && (qv[e] <= kout)) ? pv[e] : 0.f;
+            for (int e = 0; e < 4; ++e) {
+              const int cc = 16 * k + c + e;       // column inside the group's 64
+              const uint32_t w = cc < 32 ? vw0 : vw1;
+              pv[e] = ((w >> (cc & 31)) & 1u) ? pv[e] : 0.f;
+            }
           }
           // dS = P (dP - delta) scale = P (dP scale - delta scale)
           const uint64_t t01 = f2_fma(f2_pack(__uint_as_float(d_cur[c]), __uint_as_float(d_cur[c + 1])), sc2, nd01);
@@ -582,7 +612,7 @@ int launch_bwd(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k, 
         reinterpret_cast<float4*>(dqacc), n4);
   }
   BwdParams P{plan->col_ptr, plan->col_idx, plan->col_order, plan->tok_in, plan->tok_out, plan->pos,
-              plan->tile_class, lse, dlt, dqacc, reinterpret_cast<__nv_bfloat16*>(dk),
+              plan->tile_runs, plan->tile_nruns, plan->tile_class, lse, dlt, dqacc, reinterpret_cast<__nv_bfloat16*>(dk),
               reinterpret_cast<__nv_bfloat16*>(dv), status, N, T, Npad, Hq, Hkv, Hq / Hkv, scale,
               scale * 1.4426950408889634f, theta, wait_limit_ns()};
   record_timing_event(1, s);

@@ -36,7 +36,8 @@ struct FwdCfg {
   static constexpr int V_OFF = K_OFF + NS * NCH * CHUNK_BYTES;
   static constexpr int KIN_OFF = V_OFF + NS * NCH * CHUNK_BYTES;
   static constexpr int KOUT_OFF = KIN_OFF + NS * TILE * 4;
-  static constexpr int LIST_OFF = KOUT_OFF + NS * TILE * 4;    // int32 key tiles of the row
+  static constexpr int RUNS_OFF = KOUT_OFF + NS * TILE * 4;    // [NS][TREE_MAX_RUNS] int4 node runs
+  static constexpr int LIST_OFF = RUNS_OFF + NS * TREE_MAX_RUNS * 16;   // int32 key tiles of the row
   static constexpr int LCLS_OFF = LIST_OFF + kMaxList * 4;     // uint8 their tile classes
   static constexpr int BAR_OFF = LCLS_OFF + kMaxList;
   static constexpr int NBAR = 1 + 2 * NS + 3 * NH + 1;  // q, kv full/empty, s/p/o per head, drain
@@ -50,7 +51,7 @@ struct FwdCfg {
   static constexpr uint32_t TMEM_COLS = TMEM_NEED <= 256 ? 256 : 512;
   static constexpr uint32_t IDESC_S = idesc_bf16(TILE, TILE, 0, 0);   // Q K-major, K K-major
   static constexpr uint32_t IDESC_PV = idesc_bf16(TILE, HD, 0, 1);    // P (TMEM) K-major, V MN-major
-  static constexpr uint32_t KV_TX = 2 * NCH * CHUNK_BYTES + 2 * TILE * 4;
+  static constexpr uint32_t KV_TX = 2 * NCH * CHUNK_BYTES + 2 * TILE * 4 + TREE_MAX_RUNS * 16;
   static constexpr float RESCALE_THRESHOLD = 8.f;     // log2 units
 };
 
@@ -60,6 +61,8 @@ struct FwdParams {
   const int32_t* row_order;
   const int32_t* tok_in;
   const int32_t* tok_out;
+  const int32_t* tile_runs;
+  const int32_t* tile_nruns;
   const uint8_t* tile_class;
   __nv_bfloat16* o;
   float* lse;
@@ -163,6 +166,8 @@ __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
         }
         bulk_load(kin_s + s * TILE, p.tok_in + (size_t)kt * TILE, TILE * 4, &kv_full[s]);
         bulk_load(kout_s + s * TILE, p.tok_out + (size_t)kt * TILE, TILE * 4, &kv_full[s]);
+        bulk_load(sm + C::RUNS_OFF + s * TREE_MAX_RUNS * 16, p.tile_runs + (size_t)kt * TREE_MAX_RUNS * 4,
+                  TREE_MAX_RUNS * 16, &kv_full[s]);
         issued = n + 1;
       }
       if (*abort_flag) {                       // let copies in flight land before exit
@@ -255,19 +260,30 @@ __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
       tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(sv + 96));
       if (cls == 1) {                          // partial tile: tree mask in registers
         if (!mbar_wait_warp(&kv_full[s], (n / C::NS) & 1, wc)) { ok = false; break; }
-        const int4* kin4 = reinterpret_cast<const int4*>(kin_s + s * TILE);
-        const int4* kout4 = reinterpret_cast<const int4*>(kout_s + s * TILE);
-        const uint32_t ninf = __float_as_uint(-INFINITY);
+        const int nr = p.tile_nruns[kt];
         const int jrel = qi - kt * TILE;       // key c is causal-visible iff c <= jrel
-#pragma unroll
-        for (int c4 = 0; c4 < TILE / 4; ++c4) {
-          const int4 a = kin4[c4], z = kout4[c4];
-          const int c = c4 * 4;
-          if (!(c + 0 <= jrel && a.x <= qin && qin <= z.x)) sv[c + 0] = ninf;
-          if (!(c + 1 <= jrel && a.y <= qin && qin <= z.y)) sv[c + 1] = ninf;
-          if (!(c + 2 <= jrel && a.z <= qin && qin <= z.z)) sv[c + 2] = ninf;
-          if (!(c + 3 <= jrel && a.w <= qin && qin <= z.w)) sv[c + 3] = ninf;
+        uint32_t vm[4] = {0u, 0u, 0u, 0u};     // bit c: key c visible to this row
+        if (nr <= TREE_MAX_RUNS) {             // one ancestor-interval test per node run
+          const int4* runs = reinterpret_cast<const int4*>(sm + C::RUNS_OFF + s * TREE_MAX_RUNS * 16);
+          for (int k = 0; k < nr; ++k) {
+            const int4 rn = runs[k];
+            if (rn.z <= qin && qin <= rn.w) set_bits(vm, rn.x, rn.y);
+          }
+        } else {                               // many tiny nodes: test every key
+          const int4* kin4 = reinterpret_cast<const int4*>(kin_s + s * TILE);
+          const int4* kout4 = reinterpret_cast<const int4*>(kout_s + s * TILE);
+          for (int c4 = 0; c4 < TILE / 4; ++c4) {
+            const int4 a = kin4[c4], z = kout4[c4];
+            const uint32_t bits = (uint32_t)(a.x <= qin && qin <= z.x) | ((uint32_t)(a.y <= qin && qin <= z.y) << 1) |
+                                  ((uint32_t)(a.z <= qin && qin <= z.z) << 2) | ((uint32_t)(a.w <= qin && qin <= z.w) << 3);
+            vm[c4 >> 3] |= bits << (4 * (c4 & 7));
+          }
         }
+        set_bits_clear_above(vm, jrel);        // causal: keep keys c <= jrel
+        const uint32_t ninf = __float_as_uint(-INFINITY);
+#pragma unroll
+        for (int c = 0; c < TILE; ++c)
+          if (!((vm[c >> 5] >> (c & 31)) & 1u)) sv[c] = ninf;
       }
       float mx[4];
 #pragma unroll
@@ -374,7 +390,8 @@ int launch_fwd(const tree_plan_t* plan, const CUtensorMap& tq, const CUtensorMap
   int rc = record_cuda(
       cudaFuncSetAttribute(k_attn_fwd<HD, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC));
   if (rc) return rc;
-  FwdParams P{plan->row_ptr, plan->row_idx, plan->row_order, plan->tok_in, plan->tok_out, plan->tile_class,
+  FwdParams P{plan->row_ptr, plan->row_idx, plan->row_order, plan->tok_in, plan->tok_out, plan->tile_runs,
+              plan->tile_nruns, plan->tile_class,
               reinterpret_cast<__nv_bfloat16*>(o), lse, status, N, T, T * TILE, Hq, Hq / Hkv, Hq / NH,
               scale * 1.4426950408889634f, wait_limit_ns()};
   k_attn_fwd<HD, NH><<<T * (Hq / NH), C::THREADS, C::SMEM_ALLOC, s>>>(tq, tk, tv, P);

@@ -324,6 +324,35 @@ DEVI void st_swizzled_unit(uint8_t* box, int row, int unit, uint4 v) {
   *reinterpret_cast<uint4*>(box + row * 128 + phys * 16) = v;
 }
 
+// Visibility bits of a 128-key (or 128-query) tile from its node runs: run k covers tile
+// columns [start, end) and is visible when its node interval contains `x`
+// (dfs_in(run) <= x <= dfs_out(run), the ancestor test on DFS intervals); with `inner` the
+// roles swap: the run's node must lie inside [x_lo, x_hi].
+DEVI void set_bits(uint32_t (&m)[4], int a, int b) {
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const int lo = max(a, 32 * w) - 32 * w, hi = min(b, 32 * w + 32) - 32 * w;
+    if (lo < hi) m[w] |= (hi - lo == 32) ? 0xffffffffu : (((1u << (hi - lo)) - 1u) << lo);
+  }
+}
+
+// keep only bits c <= j (j < 0: none, j >= 127: all)
+DEVI void set_bits_clear_above(uint32_t (&m)[4], int j) {
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const int t = j - 32 * w;                  // highest kept bit inside word w
+    m[w] &= (t >= 31) ? 0xffffffffu : (t < 0 ? 0u : ((2u << t) - 1u));
+  }
+}
+// keep only bits c >= j (j <= 0: all, j > 127: none)
+DEVI void set_bits_clear_below(uint32_t (&m)[4], int j) {
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const int t = j - 32 * w;                  // lowest kept bit inside word w
+    m[w] &= (t <= 0) ? 0xffffffffu : (t > 31 ? 0u : ~((1u << t) - 1u));
+  }
+}
+
 // fp32 RoPE inverse frequency theta^(-2c/d); shared by the forward rotation and the
 // gradient's inverse rotation so that both use the same angles.
 DEVI float rope_inv_freq(int c, int d, float theta) {

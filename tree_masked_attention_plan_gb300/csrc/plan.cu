@@ -95,7 +95,7 @@ int node_pass(const int32_t* parent, const int32_t* node_len, int32_t n, NodePas
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
-  size_t node, tok, cls, rptr, cptr, ridx, cidx, rord, cord, hmin, hmax, cnt, total;
+  size_t node, tok, cls, rptr, cptr, ridx, cidx, rord, cord, hmin, hmax, runs, nruns, cnt, total;
 };
 
 Layout layout(int n, int N, int T) {
@@ -114,6 +114,8 @@ Layout layout(int n, int N, int T) {
   L.cord = o; o += align256(T * 4);
   L.hmin = o; o += align256(T * 4);
   L.hmax = o; o += align256(T * 4);
+  L.runs = o; o += align256((size_t)T * TREE_MAX_RUNS * 16);
+  L.nruns = o; o += align256(T * 4);
   L.cnt = o;  o += align256(4 * 4);
   L.total = o;
   (void)N;
@@ -312,6 +314,37 @@ __global__ void k_tile_fill(int T, const uint8_t* cls, const int32_t* row_ptr, i
   }
 }
 
+// One warp per tile: split the tile's 128 tokens into maximal runs of one node (a run starts
+// where dfs_in changes; padding, dfs_in = -1, is one more run) and record the first
+// TREE_MAX_RUNS of them with their node interval.  The kernels test the ancestor interval once
+// per run instead of once per token.
+__global__ void k_tile_runs(const int32_t* tok_in, const int32_t* tok_out, int32_t* runs, int32_t* nruns) {
+  const int t = blockIdx.x, lane = threadIdx.x;
+  const int32_t* in = tok_in + (size_t)t * TILE;
+  const int32_t* out = tok_out + (size_t)t * TILE;
+  int32_t* rt = runs + (size_t)t * TREE_MAX_RUNS * 4;
+  __shared__ int starts[TILE + 1];
+  int base = 0;
+  for (int ch = 0; ch < TILE / 32; ++ch) {
+    const int c = ch * 32 + lane;
+    const bool head = (c == 0) || (in[c] != in[c - 1]);
+    const unsigned m = __ballot_sync(0xffffffffu, head);
+    if (head) starts[base + __popc(m & ((1u << lane) - 1))] = c;
+    base += __popc(m);
+  }
+  __syncwarp();
+  if (lane == 0) starts[base] = TILE;
+  __syncwarp();
+  for (int k = lane; k < base && k < TREE_MAX_RUNS; k += 32) {
+    const int st = starts[k];
+    rt[4 * k + 0] = st;
+    rt[4 * k + 1] = starts[k + 1];
+    rt[4 * k + 2] = in[st];
+    rt[4 * k + 3] = out[st];
+  }
+  if (lane == 0) nruns[t] = base;
+}
+
 __global__ void k_zero_i32(int32_t* p, int n) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) p[i] = 0;
@@ -366,6 +399,8 @@ int tree_plan_bind(const tree_plan_info* info, void* buf, tree_plan_t* p) {
   p->col_order = reinterpret_cast<int32_t*>(b + L.cord);
   p->tile_hi_min = reinterpret_cast<int32_t*>(b + L.hmin);
   p->tile_hi_max = reinterpret_cast<int32_t*>(b + L.hmax);
+  p->tile_runs = reinterpret_cast<int32_t*>(b + L.runs);
+  p->tile_nruns = reinterpret_cast<int32_t*>(b + L.nruns);
   p->counts = reinterpret_cast<int32_t*>(b + L.cnt);
   p->n_nodes = n; p->n_tokens = N; p->n_tiles = T; p->n_paths = info->n_paths;
   return TREE_OK;
@@ -392,6 +427,7 @@ int tree_plan(const int32_t* parent, const int32_t* node_len, int32_t n_nodes, c
   k_plan_expand<<<(Np + 255) / 256, 256, 0, s>>>(P);
   k_zero_i32<<<1, 32, 0, s>>>(p->counts, 4);
   k_tile_hi_range<<<T, TILE, 0, s>>>(p->hi, N, p->tile_hi_min, p->tile_hi_max);
+  k_tile_runs<<<T, 32, 0, s>>>(p->tok_in, p->tok_out, p->tile_runs, p->tile_nruns);
   k_tile_rows<<<T, 256, 0, s>>>(N, T, p->tile_hi_min, p->tile_hi_max, p->tile_class, p->row_ptr + 1, p->counts);
   k_tile_cols<<<T, 256, 0, s>>>(N, T, p->tile_hi_min, p->tile_hi_max, p->col_ptr + 1);
   k_tile_scan_order<<<1, 1024, 0, s>>>(T, p->row_ptr, p->col_ptr, p->row_order, p->col_order, p->tile_hi_max);
