@@ -41,7 +41,7 @@ struct BwdCfg {
   static constexpr int LIST_OFF = RUNS_OFF + TREE_MAX_RUNS * 16; // int32 query tiles of the column
   static constexpr int LCLS_OFF = LIST_OFF + kMaxList * 4;     // uint8 their tile classes
   static constexpr int BAR_OFF = LCLS_OFF + kMaxList;
-  static constexpr int NBAR = 13;
+  static constexpr int NBAR = 16;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int SMEM = MISC_OFF + 16;
   static constexpr int SMEM_ALLOC = SMEM + 1024;
@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
   uint64_t* do_full = bars + 1;                 // dO, LSE, delta, query dfs_in of the step
   uint64_t* do_empty = bars + 2;
   uint64_t* sdp_full = bars + 3;
-  uint64_t* ds_ready = bars + 4;
+  uint64_t* ds_ready = bars + 13;               // [4] per 16-query chunk of both groups: P^T, dS^T written
   uint64_t* dq_full = bars + 5;
   uint64_t* dq_free = bars + 6;
   uint64_t* dkdv_done = bars + 7;
@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
     mbar_init(do_empty, 1);
     for (int i = 0; i < 2; ++i) { mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 1); }
     mbar_init(sdp_full, 1);
-    mbar_init(ds_ready, 256);
+    for (int i = 0; i < 4; ++i) mbar_init(&ds_ready[i], 256);
     mbar_init(dq_full, 1);
     mbar_init(dq_free, 128);
     mbar_init(dkdv_done, 1);
@@ -282,21 +282,29 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
                     C::IDESC_SDP, kk > 0 ? 1u : 0u);
         }
         umma_commit(sdp_full);
-        if (!mbar_wait(ds_ready, n & 1, wc)) { ok = false; break; }
-        tc_fence_after();
+        // dV += P^T dO and dK += dS^T Q, 16 queries (one K step) at a time as the elementwise
+        // groups finish their chunks: the tensor core works while the rest of P, dS is computed.
+        // K step kk covers queries [16 kk, 16 kk + 16): group kk / 4, chunk kk % 4.
+        for (int k = 0; k < 4; ++k) {
+          if (!mbar_wait(&ds_ready[k], n & 1, wc)) { ok = false; break; }
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < TILE / 16; ++kk) {               // dV += P^T dO (P^T from TMEM)
-          const uint32_t a_col = C::A_COL + (kk >> 2) * 64 + (kk & 3) * 8;
-          umma_bf16_tmem_a(tmem + C::DV_COL, tmem + a_col, sdesc_sw128(do_base + kk * 16 * 128, CHUNK_BYTES, 1024),
-                           C::IDESC_DKV, (n > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(do_empty);                                   // dO, LSE, delta free: next load starts
+          for (int gg = 0; gg < 2; ++gg) {
+            const int kk = 4 * gg + k;
+            umma_bf16_tmem_a(tmem + C::DV_COL, tmem + C::A_COL + 64 * gg + 8 * k,
+                             sdesc_sw128(do_base + kk * 16 * 128, CHUNK_BYTES, 1024), C::IDESC_DKV,
+                             (n > 0 || kk > 0) ? 1u : 0u);
+          }
+          if (k == 3) umma_commit(do_empty);                     // dO, LSE, delta free: next load starts
 #pragma unroll
-        for (int kk = 0; kk < TILE / 16; ++kk) {               // dK += dS^T Q
-          const uint32_t a_off = (kk >> 2) * CHUNK_BYTES + (kk & 3) * 32;
-          umma_bf16(tmem + C::DK_COL, sdesc_sw128(dst_base + a_off, 16, 1024),
-                    sdesc_sw128(q_base + kk * 16 * 128, CHUNK_BYTES, 1024), C::IDESC_DKV, (n > 0 || kk > 0) ? 1u : 0u);
+          for (int gg = 0; gg < 2; ++gg) {
+            const int kk = 4 * gg + k;
+            umma_bf16(tmem + C::DK_COL, sdesc_sw128(dst_base + gg * CHUNK_BYTES + k * 32, 16, 1024),
+                      sdesc_sw128(q_base + kk * 16 * 128, CHUNK_BYTES, 1024), C::IDESC_DKV,
+                      (n > 0 || kk > 0) ? 1u : 0u);
+          }
         }
+        if (!ok) break;
         umma_commit(&q_empty[n & 1]);                            // this Q stage free
 #pragma unroll
         for (int kk = 0; kk < TILE / 16; ++kk) {               // dQ = dS K into B (keys along K)
@@ -440,16 +448,16 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
         uint8_t* dsb = sm + C::DST_OFF + g * CHUNK_BYTES;
         st_swizzled_unit(dsb, r, 2 * k, make_uint4(dd[0], dd[1], dd[2], dd[3]));
         st_swizzled_unit(dsb, r, 2 * k + 1, make_uint4(dd[4], dd[5], dd[6], dd[7]));
+        tmem_wait_st();
+        tc_fence_before();
+        fence_proxy_async_smem();
+        mbar_arrive(&ds_ready[k]);
         if (k < 3) {
           tmem_wait_ld16x2(s_nxt, d_nxt);
 #pragma unroll
           for (int e = 0; e < 16; ++e) { s_cur[e] = s_nxt[e]; d_cur[e] = d_nxt[e]; }
         }
       }
-      tmem_wait_st();
-      tc_fence_before();
-      fence_proxy_async_smem();
-      mbar_arrive(ds_ready);
     }
     if (ok && mbar_wait_warp(dkdv_done, 0, wc)) {
       tc_fence_after();
