@@ -159,8 +159,9 @@ int tree_attn_fwd(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* 
                   const tree_bf16* v, int Hq, int Hkv, int d, float scale, tree_bf16* o,
                   float* lse, int32_t* status_dev, tree_stream_t stream);
 
-/* Bytes of device workspace tree_attn_bwd needs: delta [Hq][N_pad] fp32 followed by the
- * fp32 dQ accumulator (Hq * d * N_pad floats, one block per head and query tile). */
+/* Bytes of device workspace tree_attn_bwd needs: two fp32 [Hq][N_pad] row arrays
+ * (-delta * scale with delta_i = sum_c dO_ic O_ic, and -lse * log2(e)) followed by the fp32
+ * dQ accumulator (Hq * d * N_pad floats, one block per head and query tile). */
 size_t tree_attn_bwd_workspace(const tree_plan_t* plan, int Hq, int d);
 
 /* Backward of tree_attn_fwd (section 6.2: gradients of shared ancestors add up).

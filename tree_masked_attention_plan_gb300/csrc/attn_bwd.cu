@@ -7,14 +7,17 @@
 //                    S^T  = K Q^T            (cols   0..127, lane = key)
 //                    dP^T = V dO^T           (cols 128..255)
 //                  the elementwise warps form P^T = exp2(S^T scale log2e - LSE log2e) (masked on
-//                  partial tiles) and dS^T = P^T (dP^T - delta) scale as bf16 in shared memory;
+//                  partial tiles; packed bf16 back into cols 0..63) and dS^T = P^T (dP^T - delta)
+//                  scale as bf16 in shared memory;
 //                    dV  += P^T dO           (cols 256..256+d)     accumulated on chip,
 //                    dK  += dS^T Q           (cols 256+d..256+2d)  written once at the end,
-//                    dQ   = dS K             (cols   0..d, lane = query), added to the fp32
+//                    dQ   = dS K             (cols 128..128+d, lane = query), added to the fp32
 //                                            accumulator with coalesced red.global.add.
+//                  The steps are software-pipelined: the tensor core runs dQ, dK of step n-1,
+//                  dP, dV of step n and S of step n+1 around the elementwise passes (P, then dS).
 //                  dK gets the inverse RoPE rotation in the epilogue.
 //   k_dq_finalize  dQ = R(pos)^T dQacc, fp32 -> bf16, token-major.
-// The fp32 dQ accumulator keeps each (head, query tile) block contiguous ([d][128] per block),
+// The fp32 dQ accumulator keeps each (head, query tile) block contiguous ([d/4][128][4] per block),
 // so the reductions of the CTAs working on one query tile touch one compact region of L2.
 #include <algorithm>
 #include <cmath>
@@ -25,6 +28,9 @@ namespace ta {
 namespace {
 
 constexpr int kMaxList = 1024;      // column lists up to this length are staged in shared memory
+#ifndef BWD_L2_PREFETCH
+#define BWD_L2_PREFETCH 0
+#endif
 
 template <int HD>
 struct BwdCfg {
@@ -34,22 +40,23 @@ struct BwdCfg {
   static constexpr int Q_OFF = V_OFF + NCH * CHUNK_BYTES;     // two stages
   static constexpr int DO_OFF = Q_OFF + 2 * NCH * CHUNK_BYTES;
   static constexpr int DST_OFF = DO_OFF + NCH * CHUNK_BYTES;
-  static constexpr int LSE_OFF = DST_OFF + 2 * CHUNK_BYTES;
-  static constexpr int DLT_OFF = LSE_OFF + TILE * 4;
-  static constexpr int QIN_OFF = DLT_OFF + TILE * 4;
-  static constexpr int RUNS_OFF = QIN_OFF + TILE * 4;           // TREE_MAX_RUNS int4 node runs of the query tile
-  static constexpr int LIST_OFF = RUNS_OFF + TREE_MAX_RUNS * 16; // int32 query tiles of the column
+  // per Q stage, loaded with the Q tile: -LSE log2e, -delta scale, query dfs_in, node runs of the query tile
+  static constexpr int AUX_LSE = 0, AUX_DLT = TILE * 4, AUX_QIN = 2 * TILE * 4, AUX_RUNS = 3 * TILE * 4;
+  static constexpr int AUX_BYTES = AUX_RUNS + TREE_MAX_RUNS * 16;
+  static constexpr int AUX_OFF = DST_OFF + 2 * CHUNK_BYTES;    // two stages
+  static constexpr int STG_OFF = AUX_OFF + 2 * AUX_BYTES;      // dQ staging: 2 x [4][128][4] fp32
+  static constexpr int STG_BYTES = 16 * TILE * 4;
+  static constexpr int LIST_OFF = STG_OFF + 2 * STG_BYTES;     // int32 query tiles of the column
   static constexpr int LCLS_OFF = LIST_OFF + kMaxList * 4;     // uint8 their tile classes
   static constexpr int BAR_OFF = LCLS_OFF + kMaxList;
-  static constexpr int NBAR = 16;
+  static constexpr int NBAR = 15;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int SMEM = MISC_OFF + 16;
   static constexpr int SMEM_ALLOC = SMEM + 1024;
   // 16 warps = 4 warpgroups: [producer, MMA, 2 idle] [4 dQ drain] [4 + 4 elementwise]
   static constexpr int THREADS = 512;
   static constexpr int LAUNCH_REGS = 128;                      // 512 x 128 = the whole register file
-  static constexpr int REGS_CTRL = 48, REGS_DRAIN = 144, REGS_EW = 160;
-  static constexpr unsigned DRAIN_PACE_NS = 200;
+  static constexpr int REGS_CTRL = 88, REGS_DRAIN = 160, REGS_EW = 128;
   static_assert(128 * REGS_CTRL + 128 * REGS_DRAIN + 256 * REGS_EW <= THREADS * LAUNCH_REGS,
                 "register re-balancing must fit the launch allocation");
   static constexpr uint32_t TMEM_COLS = 512;
@@ -59,8 +66,8 @@ struct BwdCfg {
   static constexpr uint32_t IDESC_DKV = idesc_bf16(TILE, HD, 0, 1);     // P^T (TMEM) / dS^T K-major, dO/Q MN-major
   static constexpr uint32_t IDESC_DQ = idesc_bf16(TILE, HD, 1, 1);      // dS MN-major, K MN-major
   static constexpr uint32_t KV_TX = 2 * NCH * CHUNK_BYTES;
-  static constexpr uint32_t Q_TX = NCH * CHUNK_BYTES;
-  static constexpr uint32_t DO_TX = NCH * CHUNK_BYTES + 3 * TILE * 4 + TREE_MAX_RUNS * 16;
+  static constexpr uint32_t Q_TX = NCH * CHUNK_BYTES + AUX_BYTES;
+  static constexpr uint32_t DO_TX = NCH * CHUNK_BYTES;
 };
 
 struct BwdParams {
@@ -73,9 +80,9 @@ struct BwdParams {
   const int32_t* tile_runs;
   const int32_t* tile_nruns;
   const uint8_t* tile_class;
-  const float* lse;          // [Hq][Npad]
-  const float* dlt;          // [Hq][Npad]
-  float* dqacc;              // [Hq][T][HD][128]: one contiguous 64 KiB block per (head, query tile)
+  const float* nlse2;        // [Hq][Npad] -LSE log2e
+  const float* ndlt;         // [Hq][Npad] -delta scale
+  float* dqacc;              // [Hq][T][HD/4][128][4]: one contiguous 64 KiB block per (head, query tile)
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int32_t* status;
@@ -96,10 +103,11 @@ DEVI void mbar_wait_drain_b(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
 }
 
 // ------------------------------------------------------------------------------------------
-// delta and accumulator zeroing: one group of HD/8 threads per (token, q head) row
+// per query row: -delta scale (delta_i = sum_c dO_ic O_ic) and -LSE log2e; one group of HD/8
+// threads per (token, q head) row
 template <int HD>
-__global__ void k_bwd_pre(const uint4* __restrict__ o, const uint4* __restrict__ dO, float* dlt, int N, int Npad,
-                          int Hq) {
+__global__ void k_bwd_pre(const uint4* __restrict__ o, const uint4* __restrict__ dO, const float* __restrict__ lse,
+                          float* ndlt, float* nlse2, float scale, int N, int Npad, int Hq) {
   constexpr int TPR = HD / 8;
   const size_t gt = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   const size_t row = gt / TPR;                  // row = token * Hq + h
@@ -116,8 +124,11 @@ __global__ void k_bwd_pre(const uint4* __restrict__ o, const uint4* __restrict__
 #pragma unroll
   for (int off = TPR / 2; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (row < rows && sub == 0) {
+    // per query row constants of the elementwise pass, premultiplied once here
     const int h = static_cast<int>(row % Hq);
-    dlt[(size_t)h * Npad + tok] = acc;
+    const size_t at = (size_t)h * Npad + tok;
+    ndlt[at] = -acc * scale;
+    nlse2[at] = -lse[at] * 1.4426950408889634f;
   }
 }
 
@@ -137,21 +148,20 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
   uint8_t* sm = align1024b(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::BAR_OFF);
   uint64_t* kv_full = bars + 0;
-  uint64_t* do_full = bars + 1;                 // dO, LSE, delta, query dfs_in of the step
+  uint64_t* do_full = bars + 1;
   uint64_t* do_empty = bars + 2;
-  uint64_t* sdp_full = bars + 3;
-  uint64_t* ds_ready = bars + 13;               // [4] per 16-query chunk of both groups: P^T, dS^T written
+  uint64_t* s_full = bars + 3;                  // S^T(n) in A
+  uint64_t* dp_full = bars + 4;                 // dP^T(n) in B
   uint64_t* dq_full = bars + 5;
   uint64_t* dq_free = bars + 6;
   uint64_t* dkdv_done = bars + 7;
   uint64_t* drain = bars + 8;
-  uint64_t* q_full = bars + 9;                  // [2] Q stages
+  uint64_t* q_full = bars + 9;                  // [2] Q stages (with LSE, delta, dfs_in, runs)
   uint64_t* q_empty = bars + 11;                // [2]
+  uint64_t* p_ready = bars + 13;                // P^T of both groups written
+  uint64_t* ds_ready = bars + 14;               // dS^T of both groups written
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::MISC_OFF);
   int* abort_flag = reinterpret_cast<int*>(sm + C::MISC_OFF + 4);
-  const float* lse_s = reinterpret_cast<const float*>(sm + C::LSE_OFF);
-  const float* dlt_s = reinterpret_cast<const float*>(sm + C::DLT_OFF);
-  const int32_t* qin_s = reinterpret_cast<const int32_t*>(sm + C::QIN_OFF);
   int32_t* list_s = reinterpret_cast<int32_t*>(sm + C::LIST_OFF);
   uint8_t* lcls_s = sm + C::LCLS_OFF;
 
@@ -184,10 +194,12 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
     mbar_init(do_full, 1);
     mbar_init(do_empty, 1);
     for (int i = 0; i < 2; ++i) { mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 1); }
-    mbar_init(sdp_full, 1);
-    for (int i = 0; i < 4; ++i) mbar_init(&ds_ready[i], 256);
+    mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(p_ready, 8);                      // one arrival per elementwise warp
+    mbar_init(ds_ready, 8);
     mbar_init(dq_full, 1);
-    mbar_init(dq_free, 128);
+    mbar_init(dq_free, 4);                      // one arrival per drain warp
     mbar_init(dkdv_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -217,29 +229,30 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
         tma_load_3d(sm + C::K_OFF + c * CHUNK_BYTES, &tmK, kv_full, c * 64, kvh, kt * TILE);
         tma_load_3d(sm + C::V_OFF + c * CHUNK_BYTES, &tmV, kv_full, c * 64, kvh, kt * TILE);
       }
-      auto load_q = [&](int m) {               // Q tile of step m into stage m % 2
+      auto load_q = [&](int m) {               // Q tile of step m (and its row data) into stage m % 2
         int h, qt, cls;
         step_tile(m, h, qt, cls);
         uint64_t* bar = &q_full[m & 1];
         mbar_expect_tx(bar, C::Q_TX);
         for (int c = 0; c < C::NCH; ++c)
           tma_load_3d(sm + C::Q_OFF + ((m & 1) * C::NCH + c) * CHUNK_BYTES, &tmQ, bar, c * 64, h, qt * TILE);
+        uint8_t* aux = sm + C::AUX_OFF + (m & 1) * C::AUX_BYTES;
+        const size_t lo = (size_t)h * p.Npad + (size_t)qt * TILE;
+        bulk_load(aux + C::AUX_LSE, p.nlse2 + lo, TILE * 4, bar);
+        bulk_load(aux + C::AUX_DLT, p.ndlt + lo, TILE * 4, bar);
+        bulk_load(aux + C::AUX_QIN, p.tok_in + (size_t)qt * TILE, TILE * 4, bar);
+        bulk_load(aux + C::AUX_RUNS, p.tile_runs + (size_t)qt * TREE_MAX_RUNS * 4, TREE_MAX_RUNS * 16, bar);
       };
       int q_issued = 0, do_issued = 0;
       if (total > 0) { load_q(0); q_issued = 1; }
       for (int n = 0; n < total; ++n) {
         int h, qt, cls;
         step_tile(n, h, qt, cls);
-        // dO of step n once dV(n-1) has read the buffer
+        // dO of step n once dV(n-1) and dP(n-1) have read the buffer
         if (n > 0 && !mbar_wait(do_empty, (n - 1) & 1, wc)) break;
         mbar_expect_tx(do_full, C::DO_TX);
         for (int c = 0; c < C::NCH; ++c)
           tma_load_3d(sm + C::DO_OFF + c * CHUNK_BYTES, &tmDO, do_full, c * 64, h, qt * TILE);
-        const size_t lo = (size_t)h * p.Npad + (size_t)qt * TILE;
-        bulk_load(sm + C::LSE_OFF, p.lse + lo, TILE * 4, do_full);
-        bulk_load(sm + C::DLT_OFF, p.dlt + lo, TILE * 4, do_full);
-        bulk_load(sm + C::QIN_OFF, p.tok_in + (size_t)qt * TILE, TILE * 4, do_full);
-        bulk_load(sm + C::RUNS_OFF, p.tile_runs + (size_t)qt * TREE_MAX_RUNS * 4, TREE_MAX_RUNS * 16, do_full);
         do_issued = n + 1;
         // Q of step n+1 into the other stage once dK(n-1) has read it
         if (n + 1 < total) {
@@ -247,6 +260,17 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
           load_q(n + 1);
           q_issued = n + 2;
         }
+#if BWD_L2_PREFETCH
+        // Q and dO of step n+2 into L2 now, so their loads a step later do not wait on DRAM
+        if (n + 2 < total) {
+          int h2, qt2, cls2;
+          step_tile(n + 2, h2, qt2, cls2);
+          for (int c = 0; c < C::NCH; ++c) {
+            tma_prefetch_l2_3d(&tmQ, c * 64, h2, qt2 * TILE);
+            tma_prefetch_l2_3d(&tmDO, c * 64, h2, qt2 * TILE);
+          }
+        }
+#endif
       }
       if (*abort_flag) {
         mbar_wait_drain_b(kv_full, 0, p.wait_ns);
@@ -258,62 +282,75 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
+      // operand descriptors, built once: K-major (LBO unused) and MN-major (LBO = 64-element block)
       const uint32_t k_base = smem_u32(sm + C::K_OFF), v_base = smem_u32(sm + C::V_OFF);
-      const uint32_t do_base = smem_u32(sm + C::DO_OFF);
-      const uint32_t dst_base = smem_u32(sm + C::DST_OFF);
-      bool ok = mbar_wait(kv_full, 0, wc);
-      for (int n = 0; ok && n < total; ++n) {
-        const uint32_t q_base = smem_u32(sm + C::Q_OFF + (n & 1) * C::NCH * CHUNK_BYTES);
-        if (!mbar_wait(&q_full[n & 1], (n >> 1) & 1, wc)) { ok = false; break; }
+      const uint32_t do_base = smem_u32(sm + C::DO_OFF), dst_base = smem_u32(sm + C::DST_OFF);
+      const uint32_t q_base0 = smem_u32(sm + C::Q_OFF), q_base1 = q_base0 + C::NCH * CHUNK_BYTES;
+      const uint64_t k_km = sdesc_sw128(k_base, 16, 1024), k_mn = sdesc_sw128(k_base, CHUNK_BYTES, 1024);
+      const uint64_t v_km = sdesc_sw128(v_base, 16, 1024);
+      const uint64_t do_km = sdesc_sw128(do_base, 16, 1024), do_mn = sdesc_sw128(do_base, CHUNK_BYTES, 1024);
+      const uint64_t ds_km = sdesc_sw128(dst_base, 16, 1024), ds_mn = sdesc_sw128(dst_base, CHUNK_BYTES, 1024);
+      const uint64_t q_km[2] = {sdesc_sw128(q_base0, 16, 1024), sdesc_sw128(q_base1, 16, 1024)};
+      const uint64_t q_mn[2] = {sdesc_sw128(q_base0, CHUNK_BYTES, 1024), sdesc_sw128(q_base1, CHUNK_BYTES, 1024)};
+      // Software-pipelined over the steps so the tensor core runs one step's GEMMs while the
+      // elementwise warps work on the other step's tile.  A holds S^T(n), then P^T(n) until dV(n);
+      // B holds dP^T(n) until dS(n) is computed, then dQ(n) until the drain has read it.  Issue
+      // order for step n: [dQ(n-1), dK(n-1)], dP(n), dV(n), S(n+1).
+      auto issue_s = [&](int m) -> bool {       // S^T(m) = K Q(m)^T into A
+        if (!mbar_wait(&q_full[m & 1], (m >> 1) & 1, wc)) return false;
+        tc_fence_after();
+        const uint64_t qd = q_km[m & 1];
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * CHUNK_BYTES + (kk & 3) * 32;
+          umma_bf16(tmem + C::A_COL, sdesc_adv(k_km, off), sdesc_adv(qd, off), C::IDESC_SDP, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(s_full);
+        return true;
+      };
+      // dQ(m) = dS(m) K into B first, so the drain copies it out while dK += dS(m)^T Q(m) runs
+      auto issue_dq_dk = [&](int m) -> bool {
+        if (!mbar_wait(ds_ready, m & 1, wc)) return false;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {                 // S^T = K Q^T into A (after dV(n-1) read P^T)
-          const uint32_t off = (kk >> 2) * CHUNK_BYTES + (kk & 3) * 32;
-          umma_bf16(tmem + C::A_COL, sdesc_sw128(k_base + off, 16, 1024), sdesc_sw128(q_base + off, 16, 1024),
-                    C::IDESC_SDP, kk > 0 ? 1u : 0u);
-        }
-        if (n > 0 && !mbar_wait(dq_free, (n - 1) & 1, wc)) { ok = false; break; }
-        if (!mbar_wait(do_full, n & 1, wc)) { ok = false; break; }
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {                 // dP^T = V dO^T into B (dQ(n-1) drained)
-          const uint32_t off = (kk >> 2) * CHUNK_BYTES + (kk & 3) * 32;
-          umma_bf16(tmem + C::B_COL, sdesc_sw128(v_base + off, 16, 1024), sdesc_sw128(do_base + off, 16, 1024),
-                    C::IDESC_SDP, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(sdp_full);
-        // dV += P^T dO and dK += dS^T Q, 16 queries (one K step) at a time as the elementwise
-        // groups finish their chunks: the tensor core works while the rest of P, dS is computed.
-        // K step kk covers queries [16 kk, 16 kk + 16): group kk / 4, chunk kk % 4.
-        for (int k = 0; k < 4; ++k) {
-          if (!mbar_wait(&ds_ready[k], n & 1, wc)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int gg = 0; gg < 2; ++gg) {
-            const int kk = 4 * gg + k;
-            umma_bf16_tmem_a(tmem + C::DV_COL, tmem + C::A_COL + 64 * gg + 8 * k,
-                             sdesc_sw128(do_base + kk * 16 * 128, CHUNK_BYTES, 1024), C::IDESC_DKV,
-                             (n > 0 || kk > 0) ? 1u : 0u);
-          }
-          if (k == 3) umma_commit(do_empty);                     // dO, LSE, delta free: next load starts
-#pragma unroll
-          for (int gg = 0; gg < 2; ++gg) {
-            const int kk = 4 * gg + k;
-            umma_bf16(tmem + C::DK_COL, sdesc_sw128(dst_base + gg * CHUNK_BYTES + k * 32, 16, 1024),
-                      sdesc_sw128(q_base + kk * 16 * 128, CHUNK_BYTES, 1024), C::IDESC_DKV,
-                      (n > 0 || kk > 0) ? 1u : 0u);
-          }
-        }
-        if (!ok) break;
-        umma_commit(&q_empty[n & 1]);                            // this Q stage free
-#pragma unroll
-        for (int kk = 0; kk < TILE / 16; ++kk) {               // dQ = dS K into B (keys along K)
-          const uint32_t off = kk * 16 * 128;
-          umma_bf16(tmem + C::B_COL, sdesc_sw128(dst_base + off, CHUNK_BYTES, 1024),
-                    sdesc_sw128(k_base + off, CHUNK_BYTES, 1024), C::IDESC_DQ, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < TILE / 16; ++kk)
+          umma_bf16(tmem + C::B_COL, sdesc_adv(ds_mn, kk * 16 * 128), sdesc_adv(k_mn, kk * 16 * 128), C::IDESC_DQ,
+                    kk > 0 ? 1u : 0u);
         umma_commit(dq_full);
+        const uint64_t qd = q_mn[m & 1];
+#pragma unroll
+        for (int kk = 0; kk < TILE / 16; ++kk)
+          umma_bf16(tmem + C::DK_COL, sdesc_adv(ds_km, (kk >> 2) * CHUNK_BYTES + (kk & 3) * 32),
+                    sdesc_adv(qd, kk * 16 * 128), C::IDESC_DKV, (m > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&q_empty[m & 1]);                            // this Q stage free
+        return true;
+      };
+      bool ok = mbar_wait(kv_full, 0, wc);
+      if (ok && total > 0) ok = issue_s(0);
+      for (int n = 0; ok && n < total; ++n) {
+        if (n > 0 && !issue_dq_dk(n - 1)) { ok = false; break; }
+        // dP^T(n) = V dO(n)^T into B once the drain has read dQ(n-1): it runs while the
+        // elementwise warps compute P(n), so dS(n) can follow P(n) without a gap
+        if (!mbar_wait(do_full, n & 1, wc)) { ok = false; break; }
+        if (n > 0 && !mbar_wait(dq_free, (n - 1) & 1, wc)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * CHUNK_BYTES + (kk & 3) * 32;
+          umma_bf16(tmem + C::B_COL, sdesc_adv(v_km, off), sdesc_adv(do_km, off), C::IDESC_SDP, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(dp_full);
+        // dV += P(n)^T dO(n), P^T read from TMEM
+        if (!mbar_wait(p_ready, n & 1, wc)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < TILE / 16; ++kk)
+          umma_bf16_tmem_a(tmem + C::DV_COL, tmem + C::A_COL + (kk >> 2) * 64 + (kk & 3) * 8,
+                           sdesc_adv(do_mn, kk * 16 * 128), C::IDESC_DKV, (n > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(do_empty);                                   // dO(n) free once dP(n), dV(n) are done
+        if (n + 1 < total && !issue_s(n + 1)) { ok = false; break; }
       }
+      if (ok && total > 0) ok = issue_dq_dk(total - 1);
       if (ok) umma_commit(dkdv_done);
       umma_commit(drain);
       mbar_wait_drain_b(drain, 0, p.wait_ns);
@@ -322,16 +359,21 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
   } else if (warp < 8) {
     regs_inc<C::REGS_DRAIN>();
     // ---------------------------------------------------------------- dQ drain warpgroup
-    // Thread r copies dQ(n) row r (all HD columns) out of TMEM, frees the columns for dP(n+1),
-    // then adds the row into the fp32 accumulator with coalesced red.global.add (a warp
-    // instruction covers one column of 32 consecutive query rows) while the next step runs.
+    // Thread r copies dQ(n) row r (all HD columns) out of TMEM and frees the columns for
+    // dP(n+1).  The rows then go to the fp32 accumulator 16 columns (8 KiB) at a time through a
+    // double-buffered shared staging area and a bulk reduce-add by the TMA unit, while the next
+    // step runs: no per-element atomics compete with the tensor-core issue for the memory pipe.
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    float* stg = reinterpret_cast<float*>(sm + C::STG_OFF);
+    const bool leader = (threadIdx.x == 128);
+    int groups = 0;                               // bulk groups committed by the leader
     for (int n = 0; n < total; ++n) {
       int h, qt, cls;
       step_tile(n, h, qt, cls);
-      if (!mbar_wait_warp(dq_full, n & 1, wc)) break;
+      // all four warps agree before the named barriers below, so a timeout cannot split them
+      if (!named_bar_and(1, 128, mbar_wait_warp(dq_full, n & 1, wc))) break;
       tc_fence_after();
       uint32_t qv[HD];
 #pragma unroll
@@ -340,19 +382,29 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
 #pragma unroll
       for (int jc = 0; jc < HD / 32; ++jc) tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(qv + 32 * jc));
       tc_fence_before();
-      mbar_arrive(dq_free);
-      const int qi = qt * TILE + r;
-      if (qi < p.N) {
-        float* dst = p.dqacc + ((size_t)h * p.T + qt) * HD * TILE + r;
-        // paced in groups of 16 columns so the reductions spread over the next step instead of
-        // flooding the memory pipeline the elementwise warps are using at its start
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dq_free);
+      // [HD/4][128][4] block of (h, qt); rows past the last token carry exact zeros
+      float* blk = p.dqacc + ((size_t)h * p.T + qt) * HD * TILE;
 #pragma unroll
-        for (int c = 0; c < HD; ++c) {
-          atomicAdd(dst + c * TILE, __uint_as_float(qv[c]));
-          if ((c & 15) == 15 && c + 1 < HD) __nanosleep(C::DRAIN_PACE_NS);
+      for (int gi = 0; gi < HD / 16; ++gi) {
+        float* buf = stg + (gi & 1) * (C::STG_BYTES / 4);
+        if (leader && groups >= 2) bulk_wait_group_read1();   // the reduce that last read `buf` is done
+        named_bar_sync(1, 128);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint4*>(buf + (j * TILE + r) * 4) =
+              make_uint4(qv[16 * gi + 4 * j], qv[16 * gi + 4 * j + 1], qv[16 * gi + 4 * j + 2], qv[16 * gi + 4 * j + 3]);
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (leader) {
+          bulk_reduce_add_f32(blk + (size_t)gi * 4 * TILE * 4, buf, C::STG_BYTES);
+          bulk_commit_group();
+          ++groups;
         }
       }
     }
+    if (leader) bulk_wait_group0();               // every reduce has landed before the CTA ends
   } else {
     regs_inc<C::REGS_EW>();
     // ---------------------------------------------------------------- elementwise warps
@@ -371,8 +423,11 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
     for (int n = 0; n < total; ++n) {
       int h, qt, cls;
       step_tile(n, h, qt, cls);
-      if (!mbar_wait_warp(do_full, n & 1, wc) || !mbar_wait_warp(sdp_full, n & 1, wc)) { ok = false; break; }
+      if (!mbar_wait_warp(&q_full[n & 1], (n >> 1) & 1, wc) || !mbar_wait_warp(s_full, n & 1, wc)) { ok = false; break; }
       tc_fence_after();
+      const uint8_t* aux = sm + C::AUX_OFF + (n & 1) * C::AUX_BYTES;
+      const float* nlse_s = reinterpret_cast<const float*>(aux + C::AUX_LSE);
+      const float* ndlt_s = reinterpret_cast<const float*>(aux + C::AUX_DLT);
       const int jrel = j - qt * TILE;             // query i is causal-visible iff i >= jrel
       // partial tile: bits of this group's 64 query columns that key j may see, one
       // ancestor-interval test per node run of the query tile
@@ -381,12 +436,13 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
         uint32_t vm[4] = {0u, 0u, 0u, 0u};
         const int nr = p.tile_nruns[qt];
         if (nr <= TREE_MAX_RUNS) {
-          const int4* runs = reinterpret_cast<const int4*>(sm + C::RUNS_OFF);
+          const int4* runs = reinterpret_cast<const int4*>(aux + C::AUX_RUNS);
           for (int k = 0; k < nr; ++k) {
             const int4 rn = runs[k];
             if (kin <= rn.z && rn.z <= kout) set_bits(vm, rn.x, rn.y);
           }
         } else {
+          const int32_t* qin_s = reinterpret_cast<const int32_t*>(aux + C::AUX_QIN);
           for (int c4 = 0; c4 < TILE / 4; ++c4) {
             const int4 q4 = *reinterpret_cast<const int4*>(qin_s + 4 * c4);
             const uint32_t bits = (uint32_t)(kin <= q4.x && q4.x <= kout) | ((uint32_t)(kin <= q4.y && q4.y <= kout) << 1) |
@@ -399,64 +455,83 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
         vw0 = g ? vm[2] : vm[0];
         vw1 = g ? vm[3] : vm[1];
       }
-      // 4 chunks of 16 query columns; the next chunk's S^T / dP^T loads are in flight while the
-      // current chunk is computed
-      uint32_t s_cur[16], d_cur[16], s_nxt[16], d_nxt[16];
-      tmem_ld16(tmem + lane_off + C::A_COL + 64 * g, s_cur);
-      tmem_ld16(tmem + lane_off + C::B_COL + 64 * g, d_cur);
-      tmem_wait_ld16x2(s_cur, d_cur);
+      // P phase: P = exp2(S scale log2e - LSE log2e) for this group's 64 query columns: all
+      // four S^T loads in flight at once, P^T back into A as packed bf16 for dV, P kept in
+      // registers in fp32 for dS.
+      float pf[64];
+      {
+        uint32_t sv[64];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int c0 = 64 * g + 16 * k;           // first query column of this chunk
-        if (k < 3) {
-          tmem_ld16(tmem + lane_off + C::A_COL + c0 + 16, s_nxt);
-          tmem_ld16(tmem + lane_off + C::B_COL + c0 + 16, d_nxt);
-        }
-        uint32_t pp[8], dd[8];
+        for (int k = 0; k < 4; ++k)
+          tmem_ld16(tmem + lane_off + C::A_COL + 64 * g + 16 * k, *reinterpret_cast<uint32_t(*)[16]>(sv + 16 * k));
 #pragma unroll
-        for (int c = 0; c < 16; c += 4) {
-          // per column: -LSE log2e and -delta scale, in pairs
-          const float4 l4 = *reinterpret_cast<const float4*>(lse_s + c0 + c);
-          const float4 d4 = *reinterpret_cast<const float4*>(dlt_s + c0 + c);
-          const uint64_t nl01 = f2_mul(f2_pack(l4.x, l4.y), nl2e2), nl23 = f2_mul(f2_pack(l4.z, l4.w), nl2e2);
-          const uint64_t nd01 = f2_mul(f2_pack(d4.x, d4.y), nsc2), nd23 = f2_mul(f2_pack(d4.z, d4.w), nsc2);
+        for (int k = 0; k < 4; ++k) tmem_wait_ld16(*reinterpret_cast<uint32_t(*)[16]>(sv + 16 * k));
+        uint32_t pp[32];
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(nlse_s + 64 * g + c);
           float x0, x1, x2, x3;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(s_cur[c]), __uint_as_float(s_cur[c + 1])), sl2x2, nl01), x0, x1);
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(s_cur[c + 2]), __uint_as_float(s_cur[c + 3])), sl2x2, nl23), x2, x3);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2x2, f2_pack(l4.x, l4.y)), x0, x1);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), sl2x2, f2_pack(l4.z, l4.w)), x2, x3);
           float pv[4] = {ex2_approx(x0), ex2_approx(x1), ex2_approx(x2), ex2_approx(x3)};
           if (cls == 1) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int cc = 16 * k + c + e;       // column inside the group's 64
+              const int cc = c + e;                 // column inside the group's 64
               const uint32_t w = cc < 32 ? vw0 : vw1;
               pv[e] = ((w >> (cc & 31)) & 1u) ? pv[e] : 0.f;
             }
           }
-          // dS = P (dP - delta) scale = P (dP scale - delta scale)
-          const uint64_t t01 = f2_fma(f2_pack(__uint_as_float(d_cur[c]), __uint_as_float(d_cur[c + 1])), sc2, nd01);
-          const uint64_t t23 = f2_fma(f2_pack(__uint_as_float(d_cur[c + 2]), __uint_as_float(d_cur[c + 3])), sc2, nd23);
-          float e0, e1, e2, e3;
-          f2_unpack(f2_mul(f2_pack(pv[0], pv[1]), t01), e0, e1);
-          f2_unpack(f2_mul(f2_pack(pv[2], pv[3]), t23), e2, e3);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) pf[c + e] = pv[e];
           pp[c >> 1] = pack_bf16(pv[0], pv[1]);
           pp[(c >> 1) + 1] = pack_bf16(pv[2], pv[3]);
-          dd[c >> 1] = pack_bf16(e0, e1);
-          dd[(c >> 1) + 1] = pack_bf16(e2, e3);
         }
-        // P^T for these 16 queries: 8 packed columns inside this group's already-read S^T columns
-        tmem_store8(tmem + lane_off + C::A_COL + 64 * g + 8 * k, pp);
-        uint8_t* dsb = sm + C::DST_OFF + g * CHUNK_BYTES;
-        st_swizzled_unit(dsb, r, 2 * k, make_uint4(dd[0], dd[1], dd[2], dd[3]));
-        st_swizzled_unit(dsb, r, 2 * k + 1, make_uint4(dd[4], dd[5], dd[6], dd[7]));
+        // P^T: 32 packed columns over this group's (already read) S^T columns
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          tmem_store8(tmem + lane_off + C::A_COL + 64 * g + 8 * k, *reinterpret_cast<const uint32_t(*)[8]>(pp + 8 * k));
         tmem_wait_st();
         tc_fence_before();
-        fence_proxy_async_smem();
-        mbar_arrive(&ds_ready[k]);
-        if (k < 3) {
-          tmem_wait_ld16x2(s_nxt, d_nxt);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_ready);
+      }
+      // dS phase: dS = P (dP scale - delta scale), written as bf16 dS^T (keys x queries) for dK
+      // and dQ
+      if (!mbar_wait_warp(dp_full, n & 1, wc)) { ok = false; break; }
+      tc_fence_after();
+      {
+        uint8_t* dsb = sm + C::DST_OFF + g * CHUNK_BYTES;
 #pragma unroll
-          for (int e = 0; e < 16; ++e) { s_cur[e] = s_nxt[e]; d_cur[e] = d_nxt[e]; }
+        for (int half = 0; half < 2; ++half) {    // 32 query columns at a time (register budget)
+          uint32_t dv[32];
+          tmem_ld16(tmem + lane_off + C::B_COL + 64 * g + 32 * half, *reinterpret_cast<uint32_t(*)[16]>(dv));
+          tmem_ld16(tmem + lane_off + C::B_COL + 64 * g + 32 * half + 16, *reinterpret_cast<uint32_t(*)[16]>(dv + 16));
+          tmem_wait_ld16x2(*reinterpret_cast<uint32_t(*)[16]>(dv), *reinterpret_cast<uint32_t(*)[16]>(dv + 16));
+#pragma unroll
+          for (int k2 = 0; k2 < 2; ++k2) {
+            const int k = 2 * half + k2;
+            uint32_t dd[8];
+#pragma unroll
+            for (int c = 0; c < 16; c += 4) {
+              const int cc = 16 * k + c, cl = 16 * k2 + c;
+              const float4 d4 = *reinterpret_cast<const float4*>(ndlt_s + 64 * g + cc);
+              const uint64_t t01 = f2_fma(f2_pack(__uint_as_float(dv[cl]), __uint_as_float(dv[cl + 1])), sc2, f2_pack(d4.x, d4.y));
+              const uint64_t t23 = f2_fma(f2_pack(__uint_as_float(dv[cl + 2]), __uint_as_float(dv[cl + 3])), sc2, f2_pack(d4.z, d4.w));
+              float e0, e1, e2, e3;
+              f2_unpack(f2_mul(f2_pack(pf[cc], pf[cc + 1]), t01), e0, e1);
+              f2_unpack(f2_mul(f2_pack(pf[cc + 2], pf[cc + 3]), t23), e2, e3);
+              dd[c >> 1] = pack_bf16(e0, e1);
+              dd[(c >> 1) + 1] = pack_bf16(e2, e3);
+            }
+            st_swizzled_unit(dsb, r, 2 * k, make_uint4(dd[0], dd[1], dd[2], dd[3]));
+            st_swizzled_unit(dsb, r, 2 * k + 1, make_uint4(dd[4], dd[5], dd[6], dd[7]));
+          }
         }
+        tc_fence_before();                        // the dP^T reads are done before dQ rewrites B
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ds_ready);
       }
     }
     if (ok && mbar_wait_warp(dkdv_done, 0, wc)) {
@@ -527,8 +602,9 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
 
 // ------------------------------------------------------------------------------------------
 // dQ = R(pos)^T dQacc: one block per 32 tokens, all heads; angles computed once per token.
-// Per head: the [d][32] fp32 slab is read with 16-byte loads (one 128-byte line per row of
-// 32 tokens), transposed through shared memory, rotated, and written as 16-byte bf16 stores.
+// Per head: the 32 rows of the [d/4][128][4] block are read with 16-byte loads (4 columns of
+// one row each; 32 threads cover 512 contiguous bytes), transposed through shared memory,
+// rotated, and written as 16-byte bf16 stores.
 template <int HD>
 __global__ void __launch_bounds__(256) k_dq_finalize(const float* __restrict__ dqacc, const int32_t* __restrict__ pos,
                                                      __nv_bfloat16* dq, int N, int T, int Hq, float theta) {
@@ -547,14 +623,14 @@ __global__ void __launch_bounds__(256) k_dq_finalize(const float* __restrict__ d
   const int t_out = threadIdx.x / G, g_out = threadIdx.x % G;
   for (int h = 0; h < Hq; ++h) {
     __syncthreads();
-    const float* src = dqacc + ((size_t)h * T + i0 / TILE) * HD * TILE + i0 % TILE;
-    for (int e = threadIdx.x; e < HD * (TT / 4); e += blockDim.x) {
-      const int c = e / (TT / 4), t4 = e % (TT / 4);
-      const float4 v = *reinterpret_cast<const float4*>(src + (size_t)c * TILE + 4 * t4);
-      tile[c][4 * t4 + 0] = v.x;
-      tile[c][4 * t4 + 1] = v.y;
-      tile[c][4 * t4 + 2] = v.z;
-      tile[c][4 * t4 + 3] = v.w;
+    const float* src = dqacc + ((size_t)h * T + i0 / TILE) * HD * TILE + 4 * (i0 % TILE);
+    for (int e = threadIdx.x; e < (HD / 4) * TT; e += blockDim.x) {
+      const int c4 = e / TT, t = e % TT;
+      const float4 v = *reinterpret_cast<const float4*>(src + ((size_t)c4 * TILE + t) * 4);
+      tile[4 * c4 + 0][t] = v.x;
+      tile[4 * c4 + 1][t] = v.y;
+      tile[4 * c4 + 2][t] = v.z;
+      tile[4 * c4 + 3][t] = v.w;
     }
     __syncthreads();
     const int i = i0 + t_out;
@@ -589,8 +665,9 @@ int launch_bwd(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k, 
                void* ws, tree_bf16* dq, tree_bf16* dk, tree_bf16* dv, int32_t* status, cudaStream_t s) {
   using C = BwdCfg<HD>;
   const int N = plan->n_tokens, T = plan->n_tiles, Npad = T * TILE;
-  float* dlt = static_cast<float*>(ws);
-  float* dqacc = reinterpret_cast<float*>(static_cast<char*>(ws) + align256((size_t)Hq * Npad * 4));
+  float* ndlt = static_cast<float*>(ws);
+  float* nlse2 = ndlt + (size_t)Hq * Npad;
+  float* dqacc = reinterpret_cast<float*>(static_cast<char*>(ws) + align256((size_t)2 * Hq * Npad * 4));
   CUtensorMap tq, tk, tv, tdo;
   int rc = make_tmap_bf16_3d(&tq, q, HD, Hq, N);
   if (!rc) rc = make_tmap_bf16_3d(&tk, k, HD, Hkv, N);
@@ -614,13 +691,13 @@ int launch_bwd(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k, 
   {
     const size_t threads = (size_t)Npad * Hq * (HD / 8);
     k_bwd_pre<HD><<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(
-        reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dO), dlt, N, Npad, Hq);
+        reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dO), lse, ndlt, nlse2, scale, N, Npad, Hq);
     const size_t n4 = (size_t)Hq * HD * Npad / 4;
     k_zero_f32x4<<<(unsigned)std::min<size_t>((n4 + 255) / 256, 152 * 16), 256, 0, s>>>(
         reinterpret_cast<float4*>(dqacc), n4);
   }
   BwdParams P{plan->col_ptr, plan->col_idx, plan->col_order, plan->tok_in, plan->tok_out, plan->pos,
-              plan->tile_runs, plan->tile_nruns, plan->tile_class, lse, dlt, dqacc, reinterpret_cast<__nv_bfloat16*>(dk),
+              plan->tile_runs, plan->tile_nruns, plan->tile_class, nlse2, ndlt, dqacc, reinterpret_cast<__nv_bfloat16*>(dk),
               reinterpret_cast<__nv_bfloat16*>(dv), status, N, T, Npad, Hq, Hkv, Hq / Hkv, scale,
               scale * 1.4426950408889634f, theta, wait_limit_ns()};
   record_timing_event(1, s);
@@ -640,7 +717,7 @@ using namespace ta;
 extern "C" size_t tree_attn_bwd_workspace(const tree_plan_t* plan, int Hq, int d) {
   if (!plan || Hq <= 0 || d <= 0) return 0;
   const size_t Np = (size_t)plan->n_tiles * TILE;
-  return align256(Np * Hq * 4) + align256((size_t)Hq * d * Np * 4);
+  return align256(2 * Np * Hq * 4) + align256((size_t)Hq * d * Np * 4);
 }
 
 extern "C" int tree_attn_bwd(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k, const tree_bf16* v,

@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < C::NS; ++s) { mbar_init(&kv_full[s], 1); mbar_init(&kv_empty[s], 1); }
-    for (int i = 0; i < NH; ++i) { mbar_init(&s_full[i], 1); mbar_init(&p_full[i], 128); mbar_init(&o_done[i], 1); }
+    for (int i = 0; i < NH; ++i) { mbar_init(&s_full[i], 1); mbar_init(&p_full[i], 4); mbar_init(&o_done[i], 1); }
     mbar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -345,7 +345,8 @@ __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&p_full[wg]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[wg]);                 // one arrival per warp
     }
     if (ok && cnt > 0 && mbar_wait_warp(&o_done[wg], 0, wc)) {
       tc_fence_after();

@@ -131,6 +131,12 @@ DEVI bool mbar_wait_warp(uint64_t* bar, uint32_t parity, const WaitCtl& wc) {
 DEVI void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
+// warm L2 with a tile a later load will fetch (no shared memory, no completion to wait for)
+DEVI void tma_prefetch_l2_3d(const CUtensorMap* m, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(reinterpret_cast<uint64_t>(m)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
 DEVI void tma_load_3d(void* dst, const CUtensorMap* m, uint64_t* bar, int c0, int c1, int c2) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
@@ -139,6 +145,10 @@ DEVI void tma_load_3d(void* dst, const CUtensorMap* m, uint64_t* bar, int c0, in
       : "memory");
 }
 // 1-D bulk copy global -> shared; both addresses 16-byte aligned, bytes a multiple of 16
+// fire-and-forget fp32 add of 4 consecutive floats (16-byte aligned) in global memory
+DEVI void red_add_v4(float* dst, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
 DEVI void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -151,19 +161,32 @@ DEVI void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta
 
 // element-wise atomic add of a shared-memory box into global memory through a 2-D tensor map
 // (the box layout in shared memory is row-major, unswizzled); completion via bulk groups
-DEVI void tma_reduce_add_2d(const CUtensorMap* m, const void* src, int c0, int c1) {
-  asm volatile(
-      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-          reinterpret_cast<uint64_t>(m)),
-      "r"(c0), "r"(c1), "r"(smem_u32(src))
-      : "memory");
+// global[0, bytes) += shared[0, bytes) in fp32, performed by the TMA unit (16-byte aligned,
+// bytes a multiple of 16); completion tracked by the bulk groups of the issuing thread
+DEVI void bulk_reduce_add_f32(float* gdst, const void* ssrc, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(gdst),
+               "r"(smem_u32(ssrc)), "r"(bytes)
+               : "memory");
 }
 DEVI void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // wait until the shared-memory sources of every committed bulk group have been read
 DEVI void bulk_wait_group_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// ... all but the most recently committed one
+DEVI void bulk_wait_group_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 // wait until every committed bulk group has completed (its global writes performed)
 DEVI void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 DEVI void named_bar_sync(int id, int count) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory"); }
+// named barrier that also returns the AND of `pred` over the `count` participating threads
+DEVI bool named_bar_and(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
 
 // Per-warpgroup register re-balancing (all four warps of a warpgroup execute it together).
 template <int N>
@@ -233,6 +256,10 @@ DEVI uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes
   return d;
 }
 
+// The same descriptor for an address `bytes` further on (the start address field holds
+// address / 16 in 14 bits: shared-memory addresses below 256 KiB never carry out of it).
+DEVI uint64_t sdesc_adv(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
 // TMEM loads/stores, 32 data-path lanes x 32 bits, 32 consecutive columns per thread.
 // The register array is tied to the wait so that no use is scheduled before it.
 DEVI void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -292,6 +319,15 @@ DEVI void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {    // issue only; pair 
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
         "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
+}
+// waits for every tcgen05.ld of this thread issued so far; ties the register set to the wait
+DEVI void tmem_wait_ld16(uint32_t (&a)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]),
+                 "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]), "+r"(a[14]),
+                 "+r"(a[15])
+               :
+               : "memory");
 }
 // waits for every tcgen05.ld of this thread issued so far; ties both register sets to the wait
 DEVI void tmem_wait_ld16x2(uint32_t (&a)[16], uint32_t (&b)[16]) {
