@@ -9,7 +9,7 @@
 //                 dfs_in/dfs_out words) into a 2-stage ring;
 //   warp 1        allocates TMEM and issues every tcgen05.mma from one thread, head-interleaved:
 //                 O_i += P_i V(n-1), then S_i = Q_i K(n)^T, for i = 0..NH-1;
-//   warps 2+4i..  softmax warpgroup i (head i): thread r owns query row r (TMEM lane r), so the
+//   warps 4+4i..  softmax warpgroup i (head i): thread r owns query row r (TMEM lane r), so the
 //                 row max and sum never leave the thread.  It reads S_i from TMEM, masks partial
 //                 tiles with dfs_in(node j) <= dfs_in(node i) <= dfs_out(node j) (and j <= i on
 //                 the diagonal tile), and writes P_i as bf16 back into the first half of S_i's
@@ -44,7 +44,13 @@ struct FwdCfg {
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int SMEM = MISC_OFF + 16;
   static constexpr int SMEM_ALLOC = SMEM + 1024;      // slack for 1024-byte alignment
-  static constexpr int THREADS = 64 + NH * 128;
+  // warpgroup 0: producer (warp 0), MMA issuer (warp 1), two idle warps; then one softmax
+  // warpgroup per head.  With two heads the softmax warpgroups take registers from warpgroup 0.
+  static constexpr int THREADS = 128 + NH * 128;
+  static constexpr int LAUNCH_REGS = 168;             // 384 x 168 = 64512 (two heads)
+  static constexpr int REGS_CTRL = 88, REGS_SOFTMAX = 208;
+  static_assert(NH == 1 || 128 * REGS_CTRL + 256 * REGS_SOFTMAX <= THREADS * LAUNCH_REGS,
+                "register re-balancing must fit the launch allocation");
   // TMEM: S_i at columns 128 i (P_i packed bf16 in its first 64), O_i at 128 NH + HD i
   static constexpr uint32_t O_COL0 = 128 * NH;
   static constexpr uint32_t TMEM_NEED = 128 * NH + HD * NH;
@@ -141,6 +147,8 @@ __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{abort_flag, p.status, p.wait_ns};
 
+  if (warp < 4) {
+    if constexpr (NH == 2) regs_dec<C::REGS_CTRL>();
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
@@ -226,9 +234,11 @@ __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
       umma_commit(drain);                      // completes once every MMA above is done
       mbar_wait_drain(drain, 0, p.wait_ns);
     }
+  }
   } else {
+    if constexpr (NH == 2) regs_inc<C::REGS_SOFTMAX>();
     // ---------------------------------------------------------------- softmax warpgroups
-    const int wg = (warp - 2) >> 2;            // head index inside the CTA
+    const int wg = (warp - 4) >> 2;            // head index inside the CTA
     const int wq = warp & 3;                   // TMEM lane quarter this warp may access
     const int r = wq * 32 + lane;              // query row inside the tile
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
@@ -307,20 +317,20 @@ __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
       uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
       // P_i over the first 64 columns of S_i (S_i is already in registers): 64 scores per half
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
+      for (int q16 = 0; q16 < 8; ++q16) {        // 16 keys -> 8 packed columns at a time
+        uint32_t pk[8];
 #pragma unroll
-        for (int c = 64 * half; c < 64 * half + 64; c += 4) {
+        for (int c = 16 * q16; c < 16 * q16 + 16; c += 4) {
           float x0, x1, x2, x3;
           f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2x2, negm), x0, x1);
           f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), sl2x2, negm), x2, x3);
           const float e0 = ex2_approx(x0), e1 = ex2_approx(x1), e2 = ex2_approx(x2), e3 = ex2_approx(x3);
           acc0 = f2_add(acc0, f2_pack(e0, e1));
           acc1 = f2_add(acc1, f2_pack(e2, e3));
-          pk[(c - 64 * half) >> 1] = pack_bf16(e0, e1);
-          pk[((c - 64 * half) >> 1) + 1] = pack_bf16(e2, e3);
+          pk[(c - 16 * q16) >> 1] = pack_bf16(e0, e1);
+          pk[((c - 16 * q16) >> 1) + 1] = pack_bf16(e2, e3);
         }
-        tmem_store32(s_addr + 32 * half, pk);
+        tmem_store8(s_addr + 8 * q16, pk);
       }
       float a0, a1, a2, a3;
       f2_unpack(acc0, a0, a1);
@@ -395,6 +405,17 @@ int launch_fwd(const tree_plan_t* plan, const CUtensorMap& tq, const CUtensorMap
               plan->tile_nruns, plan->tile_class,
               reinterpret_cast<__nv_bfloat16*>(o), lse, status, N, T, T * TILE, Hq, Hq / Hkv, Hq / NH,
               scale * 1.4426950408889634f, wait_limit_ns()};
+  if constexpr (NH == 2) {
+    // setmaxnreg.inc waits for registers the other warpgroups released: the re-balancing only
+    // adds up if the kernel launches with exactly LAUNCH_REGS per thread.
+    cudaFuncAttributes fa;
+    rc = record_cuda(cudaFuncGetAttributes(&fa, k_attn_fwd<HD, NH>));
+    if (rc) return rc;
+    if (fa.numRegs != C::LAUNCH_REGS) {
+      record_cuda(cudaErrorInvalidConfiguration);
+      return TREE_ERR_CUDA;
+    }
+  }
   k_attn_fwd<HD, NH><<<T * (Hq / NH), C::THREADS, C::SMEM_ALLOC, s>>>(tq, tk, tv, P);
   return record_cuda(cudaGetLastError());
 }
