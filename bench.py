@@ -34,6 +34,45 @@ from workloads import CONFIGS, make_tensors, make_workload  # noqa: E402
 METRIC = "tree-attn fwd+bwd visible-pair TFLOP/s and tokens/s on 1 GB300; % of bf16 peak"
 UNIT = "TFLOP/s"
 DEFAULT_CONFIG = "rollout32k"
+# kernels of this library per step: plan (expand, zero, hi range, node runs, rows, cols, scan and
+# orders, fill), RoPE, forward, loss weights, backward (delta, zero dQ accumulator, dK/dV, dQ)
+LAUNCHES_PER_STEP = 8 + 1 + 1 + 1 + 4
+DKDV_PROFILE = os.path.join(ROOT, "profiles", "k_bwd_dkdv_rollout32k.md")
+DKDV_SOURCES = [os.path.join(ROOT, "tree_masked_attention_plan_gb300", "csrc", f) for f in ("attn_bwd.cu", "common.cuh")]
+
+
+def source_digest(paths):
+    import hashlib
+    h = hashlib.sha1()
+    for path in paths:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(config):
+    """DRAM bytes per k_bwd_dkdv launch from the committed ncu summary, if that summary was taken
+    on this workload with the kernel sources as they are now (else None: the counters are stale)."""
+    try:
+        with open(DKDV_PROFILE) as f:
+            kv = dict(line.strip().lstrip("- ").split(": ", 1) for line in f if line.strip().lstrip("- ").startswith(
+                ("source_sha1: ", "workload: ", "dram_bytes_per_launch: ")))
+    except (OSError, ValueError):
+        return None
+    if kv.get("workload") != config or kv.get("source_sha1") != source_digest(DKDV_SOURCES):
+        return None
+    try:
+        return int(float(kv["dram_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+def reduce_max(vals, device, world):
+    """Per-rank timings -> their maximum over the ranks (every rank gets the result)."""
+    t = torch.tensor([float(x) for x in vals], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t]
 
 
 def load_peaks():
@@ -284,10 +323,7 @@ def main():
     st, wl, times = res["st"], res["wl"], res["times"]
     ms = float(np.mean(times["step"]))
     ms_fwd, ms_bwd, ms_dkdv = (float(np.mean(times[x])) for x in ("fwd", "bwd", "dkdv"))
-    ms_t = torch.tensor([ms, res["e2e_ms"]], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(ms_t, op=torch.distributed.ReduceOp.MAX)
-    ms_max, e2e_max = float(ms_t[0]), float(ms_t[1])
+    ms_max, e2e_max = reduce_max([ms, res["e2e_ms"]], dev, world)
     flops = 14.0 * wl.d * wl.Hq * st["n_pairs"]
     peaks = load_peaks()
     value = world * flops / (ms_max * 1e-3) / 1e12
@@ -313,9 +349,9 @@ def main():
                     "d2h_bytes_per_step": res["d2h"]},
             "roofline": {"kernel": "k_bwd_dkdv", "bound": "tensor", "achieved": round(achieved, 2),
                          "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16"], 4),
-                         "peak_source": f"{peaks['source']} bf16 burst", "traffic": None,
+                         "peak_source": f"{peaks['source']} bf16 burst", "traffic": profiled_traffic(wl.name),
                          "algorithmic": "10 d Hq N_pairs flops per launch"},
-            "gpu_launches": 14 * args.steps,
+            "gpu_launches": LAUNCHES_PER_STEP * args.steps,
             "clocks": res["clocks"],
             "wall_s_timed_region": round(res["wall"], 3),
         }

@@ -233,6 +233,38 @@ def test_tile_classes_pairwise(tile, seed):
     assert p["nnz"] == int((cls != 0).sum()) == p["n_full"] + p["n_partial"]
 
 
+@pytest.mark.parametrize("tile", [8, 16])
+@pytest.mark.parametrize("seed", range(5))
+def test_tile_runs_rebuild_the_mask(tile, seed):
+    """The per-tile node runs partition each key tile into maximal stretches of one node, carry
+    that node's Euler interval, and the interval test over runs (plus j <= i) reproduces the
+    mask found by walking parents, for every query row against every key tile."""
+    parent, node_len = random_tree(300 + seed, n_nodes=5 + 6 * seed, max_len=9,
+                                   zero_prob=0.2, n_roots=1 + seed % 3)
+    p = oracle.plan(parent, node_len, tile=tile)
+    N, T = p["n_tokens"], p["n_tiles"]
+    for kt in range(T):
+        runs = p["tile_runs"][kt]
+        assert p["tile_nruns"][kt] == len(runs)
+        assert runs[0][0] == 0 and runs[-1][1] == tile
+        for (a, b, din, dout), nxt in zip(runs, runs[1:] + [None]):
+            assert a < b and (nxt is None or (nxt[0] == b and nxt[2] != din))
+            for j in range(kt * tile + a, kt * tile + b):
+                if j < N:
+                    v = p["tok_node"][j]
+                    assert (din, dout) == (p["dfs_in"][v], p["dfs_out"][v])
+                else:                                  # padding keys: an empty interval
+                    assert (din, dout) == (-1, -2)
+        for i in range(N):
+            anc = set(_ancestors_or_self(parent, p["tok_node"][i]))
+            qin = p["dfs_in"][p["tok_node"][i]]
+            for (a, b, din, dout) in runs:
+                for j in range(kt * tile + a, kt * tile + b):
+                    by_runs = j <= i and din <= qin <= dout
+                    by_walk = j < N and j <= i and p["tok_node"][j] in anc
+                    assert by_runs == by_walk, (i, j)
+
+
 def test_weight_double_rounding_equals_fp32_division():
     """w = float32(g/K) computed in fp64 equals IEEE fp32 division g/K (53 >= 2*24 + 2)."""
     g = np.arange(1, 700, dtype=np.int64)
