@@ -28,9 +28,6 @@ namespace ta {
 namespace {
 
 constexpr int kMaxList = 1024;      // column lists up to this length are staged in shared memory
-#ifndef BWD_L2_PREFETCH
-#define BWD_L2_PREFETCH 0
-#endif
 
 template <int HD>
 struct BwdCfg {
@@ -260,17 +257,6 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
           load_q(n + 1);
           q_issued = n + 2;
         }
-#if BWD_L2_PREFETCH
-        // Q and dO of step n+2 into L2 now, so their loads a step later do not wait on DRAM
-        if (n + 2 < total) {
-          int h2, qt2, cls2;
-          step_tile(n + 2, h2, qt2, cls2);
-          for (int c = 0; c < C::NCH; ++c) {
-            tma_prefetch_l2_3d(&tmQ, c * 64, h2, qt2 * TILE);
-            tma_prefetch_l2_3d(&tmDO, c * 64, h2, qt2 * TILE);
-          }
-        }
-#endif
       }
       if (*abort_flag) {
         mbar_wait_drain_b(kv_full, 0, p.wait_ns);
