@@ -130,6 +130,15 @@ int tree_plan_bind(const tree_plan_info* info, void* device_buffer, tree_plan_t*
 int tree_plan(const int32_t* parent, const int32_t* node_len, int32_t n_nodes,
               const tree_plan_t* plan, tree_stream_t stream);
 
+/* tree_plan for one partition of a larger tree (section 8.2 of the explainer): the tree given
+ * is the partition (its root is the cut node), and every position is shifted by pos_offset =
+ * the number of gateway tokens above it (the cut node's depth offset in the whole tree), so
+ * RoPE and the inverse rotations continue the ancestors' positions.  Everything else is the
+ * partition's own (its g and w count the partition's leaves: loss weights of a partitioned
+ * tree come from the whole tree's plan).  pos_offset < 0 -> TREE_ERR_ARG. */
+int tree_plan_offset(const int32_t* parent, const int32_t* node_len, int32_t n_nodes,
+                     int32_t pos_offset, const tree_plan_t* plan, tree_stream_t stream);
+
 /* ---------------------------------------------------------------------------------------
  * RoPE and loss weights
  * -------------------------------------------------------------------------------------*/
@@ -159,6 +168,26 @@ int tree_attn_fwd(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* 
                   const tree_bf16* v, int Hq, int Hkv, int d, float scale, tree_bf16* o,
                   float* lse, int32_t* status_dev, tree_stream_t stream);
 
+/* Gateway prefix of a partition (section 8.2 of the explainer): the K/V of the tokens on the
+ * path from the whole tree's root down to the cut node's parent, computed (and RoPE-rotated)
+ * by the partitions above and read here without recomputation.  Every token of the
+ * partition sees every gateway key: they are all its ancestors.  Gateway row r is the token
+ * at position r on that path. */
+typedef struct {
+  const tree_bf16* k;   /* [len][Hkv][d] rotated keys, path order (root first), 16-byte aligned */
+  const tree_bf16* v;   /* [len][Hkv][d]                                                      */
+  int32_t len;          /* gateway tokens, >= 1 (the partition's pos_offset)                 */
+} tree_gateway_t;
+
+/* tree_attn_fwd for a partition below a gateway: each query's softmax runs over the gateway
+ * keys (all visible, none masked but the rows past len of the last 128-key block) and its
+ * own visible keys.  `plan` is the partition's (tree_plan_offset with pos_offset = len).
+ * gw == NULL or gw->len <= 0 or a null gateway pointer -> TREE_ERR_ARG. */
+int tree_attn_fwd_gateway(const tree_plan_t* plan, const tree_gateway_t* gw, const tree_bf16* q,
+                          const tree_bf16* k, const tree_bf16* v, int Hq, int Hkv, int d,
+                          float scale, tree_bf16* o, float* lse, int32_t* status_dev,
+                          tree_stream_t stream);
+
 /* Bytes of device workspace tree_attn_bwd needs: two fp32 [Hq][N_pad] row arrays
  * (-delta * scale with delta_i = sum_c dO_ic O_ic, and -lse * log2(e)) followed by the fp32
  * dQ accumulator (Hq * d * N_pad floats, one block per head and query tile). */
@@ -176,6 +205,28 @@ int tree_attn_bwd(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* 
                   const tree_bf16* dO, int Hq, int Hkv, int d, float scale, float rope_theta,
                   void* workspace, tree_bf16* dq, tree_bf16* dk, tree_bf16* dv,
                   int32_t* status_dev, tree_stream_t stream);
+
+/* Backward of tree_attn_fwd_gateway.  Outputs as tree_attn_bwd for the partition's own tokens
+ * (dq then includes the gateway keys' contribution), plus the gateway keys' gradients from
+ * this partition's queries: dk_gw, dv_gw fp32 [len][Hkv][d], ADDED to what they hold (the
+ * fp32 accumulator that sums the children of one cut node before the relay to the parent;
+ * zero them before the first child).  dk_gw is w.r.t. the un-rotated key when
+ * rope_theta > 0 (rotated back at position r for row r).  Same workspace size as
+ * tree_attn_bwd for `plan`; dk_gw, dv_gw 16-byte aligned, else TREE_ERR_ARG. */
+int tree_attn_bwd_gateway(const tree_plan_t* plan, const tree_gateway_t* gw, const tree_bf16* q,
+                          const tree_bf16* k, const tree_bf16* v, const tree_bf16* o,
+                          const float* lse, const tree_bf16* dO, int Hq, int Hkv, int d,
+                          float scale, float rope_theta, void* workspace, tree_bf16* dq,
+                          tree_bf16* dk, tree_bf16* dv, float* dk_gw, float* dv_gw,
+                          int32_t* status_dev, tree_stream_t stream);
+
+/* The relay of section 8.2: add the fp32 gateway gradients accumulated over a cut node's
+ * children into the parent partition's bf16 dk, dv [N_parent][Hkv][d]:
+ * dk[rows[r]] += dk_gw[r] (and dv) for r < len, computed in fp32 and rounded once.
+ * rows: device int32 [len], the parent-partition token index of gateway row r (distinct).
+ * Pointers 16-byte aligned, else TREE_ERR_ARG. */
+int tree_relay_add(const int32_t* rows, int32_t len, const float* dk_gw, const float* dv_gw,
+                   int Hkv, int d, tree_bf16* dk, tree_bf16* dv, tree_stream_t stream);
 
 /* Backward without any allocation by the caller or the library (this entry point has no
  * counterpart in the Tree Training explainer; it exists for callers).  Some callers cannot

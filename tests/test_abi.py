@@ -31,7 +31,8 @@ def declared_functions():
 def test_header_declares_entry_points():
     names = declared_functions()
     for n in ("tree_plan_query", "tree_plan_bind", "tree_plan", "tree_rope_fwd", "tree_attn_fwd",
-              "tree_attn_bwd", "tree_attn_bwd_workspace", "tree_strerror"):
+              "tree_attn_bwd", "tree_attn_bwd_workspace", "tree_strerror", "tree_plan_offset",
+              "tree_attn_fwd_gateway", "tree_attn_bwd_gateway", "tree_relay_add"):
         assert n in names
 
 
@@ -103,3 +104,20 @@ def test_bind_rejects_misaligned(lib):
     for f in tam.PLAN_PTR_FIELDS:
         off = getattr(c, f) - 4096 * 16
         assert 0 <= off < info.plan_bytes and off % 4 == 0
+
+
+def test_gateway_entry_points_reject_bad_arguments_without_a_gpu(lib):
+    """Argument checks run before any CUDA call."""
+    lib.tree_relay_add.restype = ctypes.c_int
+    lib.tree_relay_add.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                   ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    assert lib.tree_relay_add(None, 4, None, None, 1, 64, None, None, None) == -6
+    lib.tree_plan_offset.restype = ctypes.c_int
+    lib.tree_plan_offset.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                     ctypes.c_void_p, ctypes.c_void_p]
+    par = np.array([-1, 0], dtype=np.int32)
+    ln = np.array([3, 4], dtype=np.int32)
+    plan = ctypes.create_string_buffer(512)
+    assert lib.tree_plan_offset(par.ctypes.data, ln.ctypes.data, 2, -1, plan, None) == -6
+    assert lib.tree_attn_fwd_gateway(None, None, None, None, None, 1, 1, 64, ctypes.c_float(0.0), None, None,
+                                     None, None) != 0

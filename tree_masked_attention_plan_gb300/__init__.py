@@ -5,8 +5,10 @@ Thin ctypes layer over ``_lib/libtreeattn.so``: it allocates outputs with PyTorc
 step of the computation runs in the library's CUDA kernels; there is no fallback.  The
 functions carry the C entry points' names (``include/tree_attn.h``):
 
-  tree_plan_query, tree_plan, tree_rope_fwd, tree_apply_weights, tree_attn_fwd,
-  tree_attn_bwd_workspace, tree_attn_bwd, tree_selftest_timeout, tree_set_wait_limit_ns
+  tree_plan_query, tree_plan (pos_offset -> tree_plan_offset), tree_rope_fwd,
+  tree_apply_weights, tree_attn_fwd, tree_attn_bwd_workspace, tree_attn_bwd,
+  tree_attn_fwd_gateway, tree_attn_bwd_gateway, tree_relay_add, tree_selftest_timeout,
+  tree_set_wait_limit_ns
 
 Semantics follow "Tree Training 技术详解" (tingdeliu.github.io): DFS packing (section 3.2),
 tree mask (4.2), block table (4.3), depth positions (5), path-count weights (6.2).
@@ -61,6 +63,10 @@ class PlanT(ctypes.Structure):
                                                       ("n_tiles", _i32), ("n_paths", _i32)]
 
 
+class Gateway(ctypes.Structure):
+    _fields_ = [("k", _vp), ("v", _vp), ("len", _i32)]
+
+
 _LIB = None
 
 
@@ -78,12 +84,18 @@ def _lib():
         "tree_plan_query": (_i32, [_vp, _vp, _i32, P(PlanInfo)]),
         "tree_plan_bind": (_i32, [P(PlanInfo), _vp, P(PlanT)]),
         "tree_plan": (_i32, [_vp, _vp, _i32, P(PlanT), _vp]),
+        "tree_plan_offset": (_i32, [_vp, _vp, _i32, _i32, P(PlanT), _vp]),
         "tree_rope_fwd": (_i32, [P(PlanT), _vp, _vp, _vp, _vp, _i32, _i32, _i32, _f32, _vp]),
         "tree_apply_weights": (_i32, [P(PlanT), _vp, _vp, _i32, _i32, _vp]),
         "tree_attn_fwd": (_i32, [P(PlanT), _vp, _vp, _vp, _i32, _i32, _i32, _f32, _vp, _vp, _vp, _vp]),
         "tree_attn_bwd_workspace": (ctypes.c_size_t, [P(PlanT), _i32, _i32]),
         "tree_attn_bwd": (_i32, [P(PlanT), _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _f32, _f32, _vp,
                                  _vp, _vp, _vp, _vp, _vp]),
+        "tree_attn_fwd_gateway": (_i32, [P(PlanT), P(Gateway), _vp, _vp, _vp, _i32, _i32, _i32, _f32, _vp, _vp,
+                                         _vp, _vp]),
+        "tree_attn_bwd_gateway": (_i32, [P(PlanT), P(Gateway), _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
+                                         _f32, _f32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+        "tree_relay_add": (_i32, [_vp, _i32, _vp, _vp, _i32, _i32, _vp, _vp, _vp]),
         "tree_set_wait_limit_ns": (_i32, [_i64]),
         "tree_set_timing_events": (_i32, [ctypes.POINTER(_vp), _i32]),
         "tree_selftest_timeout": (_i32, [_vp, _i64, _vp]),
@@ -174,8 +186,10 @@ class TreePlan:
         return out
 
 
-def tree_plan(parent, node_len, device=None, stream=None) -> TreePlan:
-    """Build the plan of a tree on the GPU (DFS order, intervals, positions, g, w, tile table)."""
+def tree_plan(parent, node_len, device=None, stream=None, pos_offset=0) -> TreePlan:
+    """Build the plan of a tree on the GPU (DFS order, intervals, positions, g, w, tile table).
+    pos_offset > 0: the tree is a partition below a gateway of that many tokens (positions
+    continue from it; tree_plan_offset)."""
     par, nl = _host_i32(parent), _host_i32(node_len)
     if par.shape != nl.shape:
         raise ValueError("parent and node_len differ in length")
@@ -187,8 +201,12 @@ def tree_plan(parent, node_len, device=None, stream=None) -> TreePlan:
     c = PlanT()
     _check(lib.tree_plan_bind(ctypes.byref(info), _ptr(buf), ctypes.byref(c)), "tree_plan_bind")
     with torch.cuda.device(dev):
-        _check(lib.tree_plan(par.ctypes.data, nl.ctypes.data, len(par), ctypes.byref(c), _stream(stream)),
-               "tree_plan")
+        if pos_offset:
+            _check(lib.tree_plan_offset(par.ctypes.data, nl.ctypes.data, len(par), int(pos_offset), ctypes.byref(c),
+                                        _stream(stream)), "tree_plan_offset")
+        else:
+            _check(lib.tree_plan(par.ctypes.data, nl.ctypes.data, len(par), ctypes.byref(c), _stream(stream)),
+                   "tree_plan")
     return TreePlan(info=info, buf=buf, c=c, device=dev)
 
 
@@ -296,3 +314,63 @@ def check_status(status, where="device"):
 __all__ = ["TreeError", "TreePlan", "tree_plan_query", "tree_plan", "tree_rope_fwd", "tree_apply_weights",
            "tree_attn_fwd", "tree_attn_bwd_workspace", "tree_attn_bwd", "tree_set_wait_limit_ns",
            "tree_selftest_timeout", "tree_set_timing_events", "new_status", "check_status", "LIB_PATH", "TILE"]
+
+
+def _gateway(k_gw, v_gw, Hkv, d):
+    if k_gw.dim() != 3:
+        raise ValueError("k_gw must be [len, Hkv, d]")
+    A = k_gw.shape[0]
+    _need(k_gw, (A, Hkv, d), torch.bfloat16, "k_gw")
+    _need(v_gw, (A, Hkv, d), torch.bfloat16, "v_gw")
+    return Gateway(k=_ptr(k_gw), v=_ptr(v_gw), len=A)
+
+
+def tree_attn_fwd_gateway(plan: TreePlan, k_gw, v_gw, q, k, v, scale=0.0, o=None, lse=None, status=None,
+                          stream=None):
+    """Forward of a partition below a gateway (ancestor K/V [len, Hkv, d], rotated, root first)."""
+    Hq, Hkv, d = _heads(plan, q, k)
+    _need(v, k.shape, torch.bfloat16, "v")
+    gw = _gateway(k_gw, v_gw, Hkv, d)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty(Hq, plan.n_pad, dtype=torch.float32, device=q.device) if lse is None else lse
+    _need(lse, (Hq, plan.n_pad), torch.float32, "lse")
+    _check(_lib().tree_attn_fwd_gateway(plan.ref(), ctypes.byref(gw), _ptr(q), _ptr(k), _ptr(v), Hq, Hkv, d,
+                                        float(scale), _ptr(o), _ptr(lse), _ptr(status), _stream(stream)),
+           "tree_attn_fwd_gateway")
+    return o, lse
+
+
+def tree_attn_bwd_gateway(plan: TreePlan, k_gw, v_gw, q, k, v, o, lse, dO, dk_gw, dv_gw, scale=0.0,
+                          rope_theta=10000.0, workspace=None, dq=None, dk=None, dv=None, status=None,
+                          stream=None):
+    """Backward of a partition below a gateway: returns (dq, dk, dv) and ADDS the gateway keys'
+    gradients from this partition into the fp32 accumulators dk_gw, dv_gw [len, Hkv, d]."""
+    Hq, Hkv, d = _heads(plan, q, k)
+    _need(v, k.shape, torch.bfloat16, "v")
+    _need(o, q.shape, torch.bfloat16, "o")
+    _need(dO, q.shape, torch.bfloat16, "dO")
+    _need(lse, (Hq, plan.n_pad), torch.float32, "lse")
+    gw = _gateway(k_gw, v_gw, Hkv, d)
+    _need(dk_gw, tuple(k_gw.shape), torch.float32, "dk_gw")
+    _need(dv_gw, tuple(k_gw.shape), torch.float32, "dv_gw")
+    if workspace is None:
+        workspace = torch.empty(tree_attn_bwd_workspace(plan, Hq, d), dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check(_lib().tree_attn_bwd_gateway(plan.ref(), ctypes.byref(gw), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                        _ptr(dO), Hq, Hkv, d, float(scale), float(rope_theta), _ptr(workspace),
+                                        _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dk_gw), _ptr(dv_gw), _ptr(status),
+                                        _stream(stream)), "tree_attn_bwd_gateway")
+    return dq, dk, dv
+
+
+def tree_relay_add(rows, dk_gw, dv_gw, dk, dv, stream=None):
+    """dk[rows[r]] += dk_gw[r] (and dv), fp32 sum rounded once to bf16; rows int32 CUDA [len]."""
+    A, Hkv, d = dk_gw.shape
+    _need(rows, (A,), torch.int32, "rows")
+    _need(dv_gw, (A, Hkv, d), torch.float32, "dv_gw")
+    _need(dk, (dk.shape[0], Hkv, d), torch.bfloat16, "dk")
+    _need(dv, tuple(dk.shape), torch.bfloat16, "dv")
+    _check(_lib().tree_relay_add(_ptr(rows), A, _ptr(dk_gw), _ptr(dv_gw), Hkv, d, _ptr(dk), _ptr(dv),
+                                 _stream(stream)), "tree_relay_add")

@@ -85,6 +85,9 @@ struct BwdParams {
   int32_t* status;
   int N, T, Npad, Hq, Hkv, grp;
   float scale, scale_log2, rope_theta;
+  int gw_len, gw_tiles;      // gateway prefix (0 = none): its key tiles get CTAs of their own
+  float* dk_gw;              // [gw_len][Hkv][HD] fp32, accumulated (+=); rotated back at pos = row
+  float* dv_gw;
   uint64_t wait_ns;
 };
 
@@ -139,6 +142,7 @@ template <int HD>
 __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
     k_bwd_dkdv(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+               const __grid_constant__ CUtensorMap tmKg, const __grid_constant__ CUtensorMap tmVg,
                const BwdParams p) {
   using C = BwdCfg<HD>;
   extern __shared__ uint8_t smem_raw[];
@@ -164,17 +168,22 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u = blockIdx.x;
-  const int kt = p.col_order[u / p.Hkv];
+  // CTAs [0, gw_tiles Hkv): gateway key tiles, seen by every query tile of the partition
+  // (they also have the longest columns, so they start first); then the own key tiles.
+  const int ngw = p.gw_tiles * p.Hkv;
+  const bool gwc = u < ngw;
+  const int kt = gwc ? u / p.Hkv : p.col_order[(u - ngw) / p.Hkv];
   const int kvh = u % p.Hkv;
-  const int cp0 = p.col_ptr[kt];
-  const int ccnt = p.col_ptr[kt + 1] - cp0;
+  const int cp0 = gwc ? 0 : p.col_ptr[kt];
+  const int ccnt = gwc ? p.T : p.col_ptr[kt + 1] - cp0;
+  const int gw_cls = (gwc && kt == p.gw_tiles - 1 && (p.gw_len % TILE) != 0) ? 1 : 2;
   const int total = ccnt * p.grp;               // steps: query tile (outer, descending) x q head (inner)
 
   // the column's query tiles and their classes, staged once
   for (int i = threadIdx.x; i < ccnt && i < kMaxList; i += blockDim.x) {
-    const int qt = p.col_idx[cp0 + i];
+    const int qt = gwc ? i : p.col_idx[cp0 + i];
     list_s[i] = qt;
-    lcls_s[i] = p.tile_class[(size_t)qt * p.T + kt];
+    lcls_s[i] = gwc ? gw_cls : p.tile_class[(size_t)qt * p.T + kt];
   }
   // step n -> (q head, query tile, class).  Query tiles are walked from the end of the column
   // with the group's q heads innermost, so CTAs running at the same time (whatever their key
@@ -183,6 +192,7 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
     const int i = ccnt - 1 - n / p.grp;
     h = kvh * p.grp + n % p.grp;
     if (i < kMaxList) { qt = list_s[i]; cls = lcls_s[i]; }
+    else if (gwc) { qt = i; cls = gw_cls; }
     else { qt = p.col_idx[cp0 + i]; cls = p.tile_class[(size_t)qt * p.T + kt]; }
   };
 
@@ -223,8 +233,8 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
       prefetch_tmap(&tmDO);
       mbar_expect_tx(kv_full, C::KV_TX);
       for (int c = 0; c < C::NCH; ++c) {
-        tma_load_3d(sm + C::K_OFF + c * CHUNK_BYTES, &tmK, kv_full, c * 64, kvh, kt * TILE);
-        tma_load_3d(sm + C::V_OFF + c * CHUNK_BYTES, &tmV, kv_full, c * 64, kvh, kt * TILE);
+        tma_load_3d(sm + C::K_OFF + c * CHUNK_BYTES, gwc ? &tmKg : &tmK, kv_full, c * 64, kvh, kt * TILE);
+        tma_load_3d(sm + C::V_OFF + c * CHUNK_BYTES, gwc ? &tmVg : &tmV, kv_full, c * 64, kvh, kt * TILE);
       }
       auto load_q = [&](int m) {               // Q tile of step m (and its row data) into stage m % 2
         int h, qt, cls;
@@ -400,8 +410,8 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
     const int wq = warp & 3;
     const int r = wq * 32 + lane;                 // key row (S^T, dP^T, dK, dV) or query row (dQ)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const int j = kt * TILE + r;
-    const int kin = p.tok_in[j], kout = p.tok_out[j];
+    const int j = kt * TILE + r;                  // key token (a gateway row in a gateway CTA)
+    const int kin = gwc ? 0 : p.tok_in[j], kout = gwc ? 0 : p.tok_out[j];
     const uint64_t nl2e2 = f2_pack(-1.4426950408889634f, -1.4426950408889634f);
     const uint64_t sl2x2 = f2_pack(p.scale_log2, p.scale_log2);
     const uint64_t sc2 = f2_pack(p.scale, p.scale), nsc2 = f2_pack(-p.scale, -p.scale);
@@ -418,7 +428,9 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
       // partial tile: bits of this group's 64 query columns that key j may see, one
       // ancestor-interval test per node run of the query tile
       uint32_t vw0 = 0xffffffffu, vw1 = 0xffffffffu;
-      if (cls == 1) {
+      if (cls == 1 && gwc) {                      // ragged gateway tile: keys past gw_len see nothing
+        vw0 = vw1 = (j < p.gw_len) ? 0xffffffffu : 0u;
+      } else if (cls == 1) {
         uint32_t vm[4] = {0u, 0u, 0u, 0u};
         const int nr = p.tile_nruns[qt];
         if (nr <= TREE_MAX_RUNS) {
@@ -520,7 +532,56 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
         if (lane == 0) mbar_arrive(ds_ready);
       }
     }
-    if (ok && mbar_wait_warp(dkdv_done, 0, wc)) {
+    if (ok && gwc && mbar_wait_warp(dkdv_done, 0, wc)) {
+      tc_fence_after();
+      // gateway row j: dV and (rotated back at position j, the row's index on the path from the
+      // root) dK added in fp32 to the caller's accumulators, which sum over child partitions
+      const bool live = j < p.gw_len;
+      float* dvg = p.dv_gw + ((size_t)j * p.Hkv + kvh) * HD;
+#pragma unroll 1
+      for (int jc = 0; jc < HD / 64; ++jc) {
+        const int c0 = (HD / 2) * g + 32 * jc;
+        uint32_t a[32];
+        tmem_load32(tmem + lane_off + C::DV_COL + c0, a);
+        if (live) {
+          float4* d4 = reinterpret_cast<float4*>(dvg + c0);
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            float4 t = d4[v];
+            t.x += __uint_as_float(a[4 * v]);
+            t.y += __uint_as_float(a[4 * v + 1]);
+            t.z += __uint_as_float(a[4 * v + 2]);
+            t.w += __uint_as_float(a[4 * v + 3]);
+            d4[v] = t;
+          }
+        }
+      }
+      float* dkg = p.dk_gw + ((size_t)j * p.Hkv + kvh) * HD;
+      const float posf = static_cast<float>(j);
+#pragma unroll 1
+      for (int jc = 0; jc < HD / 64; ++jc) {
+        const int c0 = (HD / 4) * g + 16 * jc;
+        uint32_t a[16], b[16];
+        tmem_load16(tmem + lane_off + C::DK_COL + c0, a);
+        tmem_load16(tmem + lane_off + C::DK_COL + HD / 2 + c0, b);
+        if (live) {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const float g1 = __uint_as_float(a[c]), g2 = __uint_as_float(b[c]);
+            float lo = g1, hi = g2;
+            if (p.rope_theta > 0.f) {
+              float sv, cv;
+              sincosf(posf * rope_inv_freq(c0 + c, HD, p.rope_theta), &sv, &cv);
+              lo = g1 * cv + g2 * sv;
+              hi = g2 * cv - g1 * sv;
+            }
+            dkg[c0 + c] += lo;
+            dkg[HD / 2 + c0 + c] += hi;
+          }
+        }
+      }
+    }
+    if (ok && !gwc && mbar_wait_warp(dkdv_done, 0, wc)) {
       tc_fence_after();
       // dV row j, columns [HD/2 g, HD/2 (g+1))
       __nv_bfloat16* dvrow = p.dv + ((size_t)j * p.Hkv + kvh) * HD;
@@ -648,18 +709,23 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 template <int HD>
 int launch_bwd(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k, const tree_bf16* v,
                const tree_bf16* o, const float* lse, const tree_bf16* dO, int Hq, int Hkv, float scale, float theta,
-               void* ws, tree_bf16* dq, tree_bf16* dk, tree_bf16* dv, int32_t* status, cudaStream_t s) {
+               void* ws, tree_bf16* dq, tree_bf16* dk, tree_bf16* dv, const tree_gateway_t* gw, float* dk_gw,
+               float* dv_gw, int32_t* status, cudaStream_t s) {
   using C = BwdCfg<HD>;
   const int N = plan->n_tokens, T = plan->n_tiles, Npad = T * TILE;
   float* ndlt = static_cast<float*>(ws);
   float* nlse2 = ndlt + (size_t)Hq * Npad;
   float* dqacc = reinterpret_cast<float*>(static_cast<char*>(ws) + align256((size_t)2 * Hq * Npad * 4));
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tkg, tvg;
   int rc = make_tmap_bf16_3d(&tq, q, HD, Hq, N);
   if (!rc) rc = make_tmap_bf16_3d(&tk, k, HD, Hkv, N);
   if (!rc) rc = make_tmap_bf16_3d(&tv, v, HD, Hkv, N);
   if (!rc) rc = make_tmap_bf16_3d(&tdo, dO, HD, Hq, N);
+  if (!rc && gw) rc = make_tmap_bf16_3d(&tkg, gw->k, HD, Hkv, gw->len);
+  if (!rc && gw) rc = make_tmap_bf16_3d(&tvg, gw->v, HD, Hkv, gw->len);
   if (rc) return rc;
+  if (!gw) { tkg = tk; tvg = tv; }              // unused without a gateway
+  const int A = gw ? gw->len : 0, G = (A + TILE - 1) / TILE;
   rc = record_cuda(cudaFuncSetAttribute(k_bwd_dkdv<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC));
   if (rc) return rc;
   {
@@ -685,9 +751,9 @@ int launch_bwd(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k, 
   BwdParams P{plan->col_ptr, plan->col_idx, plan->col_order, plan->tok_in, plan->tok_out, plan->pos,
               plan->tile_runs, plan->tile_nruns, plan->tile_class, nlse2, ndlt, dqacc, reinterpret_cast<__nv_bfloat16*>(dk),
               reinterpret_cast<__nv_bfloat16*>(dv), status, N, T, Npad, Hq, Hkv, Hq / Hkv, scale,
-              scale * 1.4426950408889634f, theta, wait_limit_ns()};
+              scale * 1.4426950408889634f, theta, A, G, dk_gw, dv_gw, wait_limit_ns()};
   record_timing_event(1, s);
-  k_bwd_dkdv<HD><<<T * Hkv, C::THREADS, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, P);
+  k_bwd_dkdv<HD><<<(T + G) * Hkv, C::THREADS, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, tkg, tvg, P);
   record_timing_event(2, s);
   k_dq_finalize<HD><<<(N + 31) / 32, 256, 0, s>>>(dqacc, plan->pos, reinterpret_cast<__nv_bfloat16*>(dq), N, T, Hq,
                                                   theta);
@@ -706,10 +772,12 @@ extern "C" size_t tree_attn_bwd_workspace(const tree_plan_t* plan, int Hq, int d
   return align256(2 * Np * Hq * 4) + align256((size_t)Hq * d * Np * 4);
 }
 
-extern "C" int tree_attn_bwd(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k, const tree_bf16* v,
-                             const tree_bf16* o, const float* lse, const tree_bf16* dO, int Hq, int Hkv, int d,
-                             float scale, float rope_theta, void* workspace, tree_bf16* dq, tree_bf16* dk,
-                             tree_bf16* dv, int32_t* status_dev, tree_stream_t stream) {
+namespace ta {
+namespace {
+int bwd_entry(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k, const tree_bf16* v,
+              const tree_bf16* o, const float* lse, const tree_bf16* dO, int Hq, int Hkv, int d, float scale,
+              float rope_theta, void* workspace, tree_bf16* dq, tree_bf16* dk, tree_bf16* dv,
+              const tree_gateway_t* gw, float* dk_gw, float* dv_gw, int32_t* status_dev, tree_stream_t stream) {
   int rc = plan_ok(plan);
   if (rc) return rc;
   if (!q || !k || !v || !o || !lse || !dO || !workspace || !dq || !dk || !dv) return TREE_ERR_ARG;
@@ -717,14 +785,68 @@ extern "C" int tree_attn_bwd(const tree_plan_t* plan, const tree_bf16* q, const 
   for (const void* ptr : {(const void*)o, (const void*)dO, (const void*)dq, (const void*)dk, (const void*)dv})
     if (reinterpret_cast<uintptr_t>(ptr) & 15) return TREE_ERR_ARG;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255) || (reinterpret_cast<uintptr_t>(lse) & 15)) return TREE_ERR_ARG;
+  if (gw && (!gw->k || !gw->v || gw->len <= 0 || !dk_gw || !dv_gw || (reinterpret_cast<uintptr_t>(dk_gw) & 15) ||
+             (reinterpret_cast<uintptr_t>(dv_gw) & 15)))
+    return TREE_ERR_ARG;
   rc = check_device();
   if (rc) return rc;
   if (!(scale > 0.f)) scale = 1.f / sqrtf(static_cast<float>(d));
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return d == 128 ? launch_bwd<128>(plan, q, k, v, o, lse, dO, Hq, Hkv, scale, rope_theta, workspace, dq, dk, dv,
-                                    status_dev, s)
-                  : launch_bwd<64>(plan, q, k, v, o, lse, dO, Hq, Hkv, scale, rope_theta, workspace, dq, dk, dv,
-                                   status_dev, s);
+  return d == 128 ? launch_bwd<128>(plan, q, k, v, o, lse, dO, Hq, Hkv, scale, rope_theta, workspace, dq, dk, dv, gw,
+                                    dk_gw, dv_gw, status_dev, s)
+                  : launch_bwd<64>(plan, q, k, v, o, lse, dO, Hq, Hkv, scale, rope_theta, workspace, dq, dk, dv, gw,
+                                   dk_gw, dv_gw, status_dev, s);
+}
+
+// parent rows += fp32 gateway gradients, one thread per 8 columns of a (row, kv head)
+__global__ void k_relay_add(const int32_t* __restrict__ rows, int A, const float* __restrict__ gk,
+                            const float* __restrict__ gv, __nv_bfloat16* dk, __nv_bfloat16* dv, int HkvD) {
+  const size_t e = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;
+  if (e >= (size_t)A * HkvD) return;
+  const size_t r = e / HkvD, c = e % HkvD;
+  const size_t dst = (size_t)rows[r] * HkvD + c;
+  for (int which = 0; which < 2; ++which) {
+    const float* src = (which ? gv : gk) + e;
+    uint4* out = reinterpret_cast<uint4*>((which ? dv : dk) + dst);
+    const uint4 cur = *out;
+    const float4 a = *reinterpret_cast<const float4*>(src), b = *reinterpret_cast<const float4*>(src + 4);
+    *out = make_uint4(pack_bf16(bf16lo(cur.x) + a.x, bf16hi(cur.x) + a.y), pack_bf16(bf16lo(cur.y) + a.z, bf16hi(cur.y) + a.w),
+                      pack_bf16(bf16lo(cur.z) + b.x, bf16hi(cur.z) + b.y), pack_bf16(bf16lo(cur.w) + b.z, bf16hi(cur.w) + b.w));
+  }
+}
+}  // namespace
+}  // namespace ta
+
+extern "C" int tree_attn_bwd(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k, const tree_bf16* v,
+                             const tree_bf16* o, const float* lse, const tree_bf16* dO, int Hq, int Hkv, int d,
+                             float scale, float rope_theta, void* workspace, tree_bf16* dq, tree_bf16* dk,
+                             tree_bf16* dv, int32_t* status_dev, tree_stream_t stream) {
+  return bwd_entry(plan, q, k, v, o, lse, dO, Hq, Hkv, d, scale, rope_theta, workspace, dq, dk, dv, nullptr, nullptr,
+                   nullptr, status_dev, stream);
+}
+
+extern "C" int tree_attn_bwd_gateway(const tree_plan_t* plan, const tree_gateway_t* gw, const tree_bf16* q,
+                                     const tree_bf16* k, const tree_bf16* v, const tree_bf16* o, const float* lse,
+                                     const tree_bf16* dO, int Hq, int Hkv, int d, float scale, float rope_theta,
+                                     void* workspace, tree_bf16* dq, tree_bf16* dk, tree_bf16* dv, float* dk_gw,
+                                     float* dv_gw, int32_t* status_dev, tree_stream_t stream) {
+  if (!gw) return TREE_ERR_ARG;
+  return bwd_entry(plan, q, k, v, o, lse, dO, Hq, Hkv, d, scale, rope_theta, workspace, dq, dk, dv, gw, dk_gw, dv_gw,
+                   status_dev, stream);
+}
+
+extern "C" int tree_relay_add(const int32_t* rows, int32_t len, const float* dk_gw, const float* dv_gw, int Hkv,
+                              int d, tree_bf16* dk, tree_bf16* dv, tree_stream_t stream) {
+  if (!rows || !dk_gw || !dv_gw || !dk || !dv || len <= 0) return TREE_ERR_ARG;
+  if ((d != 64 && d != 128) || Hkv <= 0) return TREE_ERR_SHAPE;
+  for (const void* ptr : {(const void*)dk_gw, (const void*)dv_gw, (const void*)dk, (const void*)dv})
+    if (reinterpret_cast<uintptr_t>(ptr) & 15) return TREE_ERR_ARG;
+  int rc = check_device();
+  if (rc) return rc;
+  const size_t groups = (size_t)len * Hkv * d / 8;
+  k_relay_add<<<(unsigned)((groups + 255) / 256), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      rows, len, dk_gw, dv_gw, reinterpret_cast<__nv_bfloat16*>(dk), reinterpret_cast<__nv_bfloat16*>(dv), Hkv * d);
+  return record_cuda(cudaGetLastError());
 }
 
 // ------------------------------------------------------------------------------------------

@@ -58,6 +58,7 @@ struct FwdCfg {
   static constexpr uint32_t IDESC_S = idesc_bf16(TILE, TILE, 0, 0);   // Q K-major, K K-major
   static constexpr uint32_t IDESC_PV = idesc_bf16(TILE, HD, 0, 1);    // P (TMEM) K-major, V MN-major
   static constexpr uint32_t KV_TX = 2 * NCH * CHUNK_BYTES + 2 * TILE * 4 + TREE_MAX_RUNS * 16;
+  static constexpr uint32_t KVG_TX = 2 * NCH * CHUNK_BYTES;           // a gateway tile: K, V only
   static constexpr float RESCALE_THRESHOLD = 8.f;     // log2 units
 };
 
@@ -74,6 +75,7 @@ struct FwdParams {
   float* lse;
   int32_t* status;
   int N, T, Npad, Hq, grp, n_hgroups;
+  int gw_len, gw_tiles;      // gateway prefix: keys every query sees (0 = none), its 128-key tiles
   float scale_log2;          // softmax scale * log2(e)
   uint64_t wait_ns;
 };
@@ -90,10 +92,13 @@ DEVI void mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
     if (global_timer_ns() - t0 > limit_ns) return;
 }
 
-template <int HD, int NH>
+// GW: the instantiation with gateway tiles in front of each row (the plain tree keeps the
+// code without the gateway branches)
+template <int HD, int NH, bool GW>
 __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
     k_attn_fwd(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-               const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmKg,
+               const __grid_constant__ CUtensorMap tmVg, const FwdParams p) {
   using C = FwdCfg<HD, NH>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
@@ -116,15 +121,21 @@ __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
   const int h0 = (u % p.n_hgroups) * NH;              // first q head of this CTA
   const int kvh = h0 / p.grp;
   const int rp0 = p.row_ptr[qt];
-  const int cnt = p.row_ptr[qt + 1] - rp0;
+  const int rcnt = p.row_ptr[qt + 1] - rp0;
+  const int G = GW ? p.gw_tiles : 0;
+  const int cnt = G + rcnt;                           // gateway tiles first, then the row's own
   int32_t* list_s = reinterpret_cast<int32_t*>(sm + C::LIST_OFF);
   uint8_t* lcls_s = sm + C::LCLS_OFF;
-  for (int i = threadIdx.x; i < cnt && i < kMaxList; i += blockDim.x) {   // the row's key tiles, staged once
+  for (int i = threadIdx.x; i < rcnt && i < kMaxList; i += blockDim.x) {   // the row's key tiles, staged once
     const int kt = p.row_idx[rp0 + i];
     list_s[i] = kt;
     lcls_s[i] = p.tile_class[(size_t)qt * p.T + kt];
   }
+  // step n -> key tile and class; gateway tile n < G: every key before gw_len is visible (the
+  // last one is partial when gw_len is not a multiple of 128: keys past gw_len are masked)
   auto row_tile = [&](int n, int& kt, int& cls) {
+    if (GW && n < G) { kt = n; cls = (n == G - 1 && (p.gw_len % TILE) != 0) ? 1 : 2; return; }
+    n -= G;
     if (n < kMaxList) { kt = list_s[n]; cls = lcls_s[n]; }
     else { kt = p.row_idx[rp0 + n]; cls = p.tile_class[(size_t)qt * p.T + kt]; }
   };
@@ -155,6 +166,10 @@ __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
+      if (GW) {
+        prefetch_tmap(&tmKg);
+        prefetch_tmap(&tmVg);
+      }
       mbar_expect_tx(q_full, NH * C::NCH * CHUNK_BYTES);
       for (int i = 0; i < NH; ++i)
         for (int c = 0; c < C::NCH; ++c)
@@ -165,9 +180,18 @@ __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
         if (n >= C::NS && !mbar_wait(&kv_empty[s], ((n / C::NS) - 1) & 1, wc)) break;
         int kt, cls;
         row_tile(n, kt, cls);
-        mbar_expect_tx(&kv_full[s], C::KV_TX);
         uint8_t* kb = sm + C::K_OFF + s * C::NCH * CHUNK_BYTES;
         uint8_t* vb = sm + C::V_OFF + s * C::NCH * CHUNK_BYTES;
+        if (GW && n < G) {                     // gateway tile: K, V only (rows past gw_len read as 0)
+          mbar_expect_tx(&kv_full[s], C::KVG_TX);
+          for (int c = 0; c < C::NCH; ++c) {
+            tma_load_3d(kb + c * CHUNK_BYTES, &tmKg, &kv_full[s], c * 64, kvh, kt * TILE);
+            tma_load_3d(vb + c * CHUNK_BYTES, &tmVg, &kv_full[s], c * 64, kvh, kt * TILE);
+          }
+          issued = n + 1;
+          continue;
+        }
+        mbar_expect_tx(&kv_full[s], C::KV_TX);
         for (int c = 0; c < C::NCH; ++c) {
           tma_load_3d(kb + c * CHUNK_BYTES, &tmK, &kv_full[s], c * 64, kvh, kt * TILE);
           tma_load_3d(vb + c * CHUNK_BYTES, &tmV, &kv_full[s], c * 64, kvh, kt * TILE);
@@ -268,7 +292,14 @@ __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
       tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(sv + 32));
       tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(sv + 64));
       tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(sv + 96));
-      if (cls == 1) {                          // partial tile: tree mask in registers
+      if (GW && cls == 1 && n < G) {           // ragged last gateway tile: keys past gw_len
+        uint32_t vm[4] = {0u, 0u, 0u, 0u};
+        set_bits(vm, 0, p.gw_len - kt * TILE);
+        const uint32_t ninf = __float_as_uint(-INFINITY);
+#pragma unroll
+        for (int c = 0; c < TILE; ++c)
+          if (!((vm[c >> 5] >> (c & 31)) & 1u)) sv[c] = ninf;
+      } else if (cls == 1) {                   // partial tile: tree mask in registers
         if (!mbar_wait_warp(&kv_full[s], (n / C::NS) & 1, wc)) { ok = false; break; }
         const int nr = p.tile_nruns[kt];
         const int jrel = qi - kt * TILE;       // key c is causal-visible iff c <= jrel
@@ -393,30 +424,31 @@ __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
   }
 }
 
-template <int HD, int NH>
-int launch_fwd(const tree_plan_t* plan, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, int Hq,
-               int Hkv, float scale, tree_bf16* o, float* lse, int32_t* status, cudaStream_t s) {
+template <int HD, int NH, bool GW>
+int launch_fwd(const tree_plan_t* plan, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+               const CUtensorMap& tkg, const CUtensorMap& tvg, int gw_len, int Hq, int Hkv, float scale, tree_bf16* o,
+               float* lse, int32_t* status, cudaStream_t s) {
   using C = FwdCfg<HD, NH>;
   const int N = plan->n_tokens, T = plan->n_tiles;
   int rc = record_cuda(
-      cudaFuncSetAttribute(k_attn_fwd<HD, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC));
+      cudaFuncSetAttribute(k_attn_fwd<HD, NH, GW>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC));
   if (rc) return rc;
   FwdParams P{plan->row_ptr, plan->row_idx, plan->row_order, plan->tok_in, plan->tok_out, plan->tile_runs,
               plan->tile_nruns, plan->tile_class,
               reinterpret_cast<__nv_bfloat16*>(o), lse, status, N, T, T * TILE, Hq, Hq / Hkv, Hq / NH,
-              scale * 1.4426950408889634f, wait_limit_ns()};
+              gw_len, (gw_len + TILE - 1) / TILE, scale * 1.4426950408889634f, wait_limit_ns()};
   if constexpr (NH == 2) {
     // setmaxnreg.inc waits for registers the other warpgroups released: the re-balancing only
     // adds up if the kernel launches with exactly LAUNCH_REGS per thread.
     cudaFuncAttributes fa;
-    rc = record_cuda(cudaFuncGetAttributes(&fa, k_attn_fwd<HD, NH>));
+    rc = record_cuda(cudaFuncGetAttributes(&fa, k_attn_fwd<HD, NH, GW>));
     if (rc) return rc;
     if (fa.numRegs != C::LAUNCH_REGS) {
       record_cuda(cudaErrorInvalidConfiguration);
       return TREE_ERR_CUDA;
     }
   }
-  k_attn_fwd<HD, NH><<<T * (Hq / NH), C::THREADS, C::SMEM_ALLOC, s>>>(tq, tk, tv, P);
+  k_attn_fwd<HD, NH, GW><<<T * (Hq / NH), C::THREADS, C::SMEM_ALLOC, s>>>(tq, tk, tv, tkg, tvg, P);
   return record_cuda(cudaGetLastError());
 }
 
@@ -425,28 +457,57 @@ int launch_fwd(const tree_plan_t* plan, const CUtensorMap& tq, const CUtensorMap
 
 using namespace ta;
 
-extern "C" int tree_attn_fwd(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k, const tree_bf16* v,
-                             int Hq, int Hkv, int d, float scale, tree_bf16* o, float* lse, int32_t* status_dev,
-                             tree_stream_t stream) {
+namespace ta {
+namespace {
+int fwd_entry(const tree_plan_t* plan, const tree_gateway_t* gw, const tree_bf16* q, const tree_bf16* k,
+              const tree_bf16* v, int Hq, int Hkv, int d, float scale, tree_bf16* o, float* lse, int32_t* status_dev,
+              tree_stream_t stream) {
   int rc = plan_ok(plan);
   if (rc) return rc;
   if (!q || !k || !v || !o || !lse) return TREE_ERR_ARG;
   if ((d != 64 && d != 128) || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return TREE_ERR_SHAPE;
   if ((reinterpret_cast<uintptr_t>(o) & 15) || (reinterpret_cast<uintptr_t>(lse) & 3)) return TREE_ERR_ARG;
+  if (gw && (!gw->k || !gw->v || gw->len <= 0)) return TREE_ERR_ARG;
   rc = check_device();
   if (rc) return rc;
   if (!(scale > 0.f)) scale = 1.f / sqrtf(static_cast<float>(d));
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int N = plan->n_tokens;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, tkg, tvg;
   rc = make_tmap_bf16_3d(&tq, q, d, Hq, N);
   if (!rc) rc = make_tmap_bf16_3d(&tk, k, d, Hkv, N);
   if (!rc) rc = make_tmap_bf16_3d(&tv, v, d, Hkv, N);
+  if (!rc && gw) rc = make_tmap_bf16_3d(&tkg, gw->k, d, Hkv, gw->len);
+  if (!rc && gw) rc = make_tmap_bf16_3d(&tvg, gw->v, d, Hkv, gw->len);
   if (rc) return rc;
+  if (!gw) { tkg = tk; tvg = tv; }              // unused without a gateway
+  const int A = gw ? gw->len : 0;
   const bool pair = ((Hq / Hkv) % 2) == 0;   // two q heads of one kv group per CTA
+  if (gw) {
+    if (d == 128)
+      return pair ? launch_fwd<128, 2, true>(plan, tq, tk, tv, tkg, tvg, A, Hq, Hkv, scale, o, lse, status_dev, s)
+                  : launch_fwd<128, 1, true>(plan, tq, tk, tv, tkg, tvg, A, Hq, Hkv, scale, o, lse, status_dev, s);
+    return pair ? launch_fwd<64, 2, true>(plan, tq, tk, tv, tkg, tvg, A, Hq, Hkv, scale, o, lse, status_dev, s)
+                : launch_fwd<64, 1, true>(plan, tq, tk, tv, tkg, tvg, A, Hq, Hkv, scale, o, lse, status_dev, s);
+  }
   if (d == 128)
-    return pair ? launch_fwd<128, 2>(plan, tq, tk, tv, Hq, Hkv, scale, o, lse, status_dev, s)
-                : launch_fwd<128, 1>(plan, tq, tk, tv, Hq, Hkv, scale, o, lse, status_dev, s);
-  return pair ? launch_fwd<64, 2>(plan, tq, tk, tv, Hq, Hkv, scale, o, lse, status_dev, s)
-              : launch_fwd<64, 1>(plan, tq, tk, tv, Hq, Hkv, scale, o, lse, status_dev, s);
+    return pair ? launch_fwd<128, 2, false>(plan, tq, tk, tv, tkg, tvg, 0, Hq, Hkv, scale, o, lse, status_dev, s)
+                : launch_fwd<128, 1, false>(plan, tq, tk, tv, tkg, tvg, 0, Hq, Hkv, scale, o, lse, status_dev, s);
+  return pair ? launch_fwd<64, 2, false>(plan, tq, tk, tv, tkg, tvg, 0, Hq, Hkv, scale, o, lse, status_dev, s)
+              : launch_fwd<64, 1, false>(plan, tq, tk, tv, tkg, tvg, 0, Hq, Hkv, scale, o, lse, status_dev, s);
+}
+}  // namespace
+}  // namespace ta
+
+extern "C" int tree_attn_fwd(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k, const tree_bf16* v,
+                             int Hq, int Hkv, int d, float scale, tree_bf16* o, float* lse, int32_t* status_dev,
+                             tree_stream_t stream) {
+  return fwd_entry(plan, nullptr, q, k, v, Hq, Hkv, d, scale, o, lse, status_dev, stream);
+}
+
+extern "C" int tree_attn_fwd_gateway(const tree_plan_t* plan, const tree_gateway_t* gw, const tree_bf16* q,
+                                     const tree_bf16* k, const tree_bf16* v, int Hq, int Hkv, int d, float scale,
+                                     tree_bf16* o, float* lse, int32_t* status_dev, tree_stream_t stream) {
+  if (!gw) return TREE_ERR_ARG;
+  return fwd_entry(plan, gw, q, k, v, Hq, Hkv, d, scale, o, lse, status_dev, stream);
 }

@@ -130,6 +130,7 @@ struct PlanDev {
   int32_t *tok_node, *pos, *g, *tok_in, *tok_out, *hi;
   float* w;
   int n, N, T, K;
+  int pos0;                 // position of the first token of every root (0, or a gateway's length)
 };
 
 // a2: one thread per packed token (padding included).  The token's node is the last node
@@ -151,7 +152,7 @@ __global__ void k_plan_expand(PlanDev P) {
   const int v = P.order[lo];
   const int gv = P.leaves[v];
   P.tok_node[t] = v;
-  P.pos[t] = P.depth_off[v] + (t - P.tok_start[v]);
+  P.pos[t] = P.pos0 + P.depth_off[v] + (t - P.tok_start[v]);
   P.g[t] = gv;
   P.w[t] = __fdiv_rn(static_cast<float>(gv), static_cast<float>(P.K));
   P.tok_in[t] = P.dfs_in[v];
@@ -408,7 +409,12 @@ int tree_plan_bind(const tree_plan_info* info, void* buf, tree_plan_t* p) {
 
 int tree_plan(const int32_t* parent, const int32_t* node_len, int32_t n_nodes, const tree_plan_t* p,
               tree_stream_t stream_) {
-  if (!p) return TREE_ERR_ARG;
+  return tree_plan_offset(parent, node_len, n_nodes, 0, p, stream_);
+}
+
+int tree_plan_offset(const int32_t* parent, const int32_t* node_len, int32_t n_nodes, int32_t pos_offset,
+                     const tree_plan_t* p, tree_stream_t stream_) {
+  if (!p || pos_offset < 0) return TREE_ERR_ARG;
   NodePass np;
   int rc = node_pass(parent, node_len, n_nodes, &np);
   if (rc) return rc;
@@ -422,7 +428,7 @@ int tree_plan(const int32_t* parent, const int32_t* node_len, int32_t n_nodes, c
   rc = record_cuda(cudaMemcpyAsync(p->order, np.block.data(), np.block.size() * 4, cudaMemcpyHostToDevice, s));
   if (rc) return rc;
   PlanDev P{p->order, p->dfs_in, p->dfs_out, p->tok_start, p->depth_off, p->leaves, p->dfs_tok_start,
-            p->sub_end, p->tok_node, p->pos, p->g, p->tok_in, p->tok_out, p->hi, p->w, n, N, T, np.K};
+            p->sub_end, p->tok_node, p->pos, p->g, p->tok_in, p->tok_out, p->hi, p->w, n, N, T, np.K, pos_offset};
   const int Np = T * TILE;
   k_plan_expand<<<(Np + 255) / 256, 256, 0, s>>>(P);
   k_zero_i32<<<1, 32, 0, s>>>(p->counts, 4);
