@@ -228,6 +228,13 @@ int tree_attn_bwd_gateway(const tree_plan_t* plan, const tree_gateway_t* gw, con
 int tree_relay_add(const int32_t* rows, int32_t len, const float* dk_gw, const float* dv_gw,
                    int Hkv, int d, tree_bf16* dk, tree_bf16* dv, tree_stream_t stream);
 
+/* dst[r] = src[rows[r]] for r < n: bf16 rows of row_elems elements (a multiple of 8), e.g.
+ * the gateway K/V of a child partition gathered from the parent partition's rotated k and v
+ * (row_elems = Hkv * d).  rows: device int32 [n]; src, dst 16-byte aligned, else
+ * TREE_ERR_ARG. */
+int tree_gather_rows(const int32_t* rows, int32_t n, const tree_bf16* src, tree_bf16* dst,
+                     int row_elems, tree_stream_t stream);
+
 /* Backward without any allocation by the caller or the library (this entry point has no
  * counterpart in the Tree Training explainer; it exists for callers).  Some callers cannot
  * provide the workspace tree_attn_bwd needs: code that drives this library through the plain

@@ -83,3 +83,19 @@ def test_relay_is_the_sum_of_the_partition_losses(seed, gw, max_len, n_extra):
     # the child loss reaches parent-partition keys only through the gateway (the path)
     off_path = np.setdiff1d(P["parent"].tokens, P["gw_tokens"])
     assert np.abs(b["dk"][off_path]).max() == 0 and np.abs(b["dv"][off_path]).max() == 0
+
+
+@pytest.mark.parametrize("seed,gw,max_len,n_extra", CASES)
+def test_library_partitioner_matches_the_test_bookkeeping(seed, gw, max_len, n_extra):
+    """The package's host partitioner (own depth-first packing) against the oracle-plan-based
+    bookkeeping of these tests."""
+    from tree_masked_attention_plan_gb300.partition import partition_tree
+    parent, lens, cut = gateway_tree(seed, gw, branch_len=23, n_extra=n_extra, max_len=max_len)
+    P, Q = partition(parent, lens, cut), partition_tree(parent, lens, cut)
+    assert P["A"] == Q["A"]
+    assert np.array_equal(P["gw_tokens"], Q["gw_tokens"]) and np.array_equal(P["gw_rows"], Q["gw_rows"])
+    kids = [c for c in P["children"] if c.node_len.sum() > 0]
+    assert len(kids) == len(Q["children"])
+    for a, b in zip([P["parent"]] + kids, [Q["parent"]] + Q["children"]):
+        assert np.array_equal(a.parent, b.parent) and np.array_equal(a.node_len, b.node_len)
+        assert np.array_equal(a.tokens, b.tokens) and a.pos_offset == b.pos_offset

@@ -7,7 +7,7 @@ functions carry the C entry points' names (``include/tree_attn.h``):
 
   tree_plan_query, tree_plan (pos_offset -> tree_plan_offset), tree_rope_fwd,
   tree_apply_weights, tree_attn_fwd, tree_attn_bwd_workspace, tree_attn_bwd,
-  tree_attn_fwd_gateway, tree_attn_bwd_gateway, tree_relay_add, tree_selftest_timeout,
+  tree_attn_fwd_gateway, tree_attn_bwd_gateway, tree_relay_add, tree_gather_rows, tree_selftest_timeout,
   tree_set_wait_limit_ns
 
 Semantics follow "Tree Training 技术详解" (tingdeliu.github.io): DFS packing (section 3.2),
@@ -96,6 +96,7 @@ def _lib():
         "tree_attn_bwd_gateway": (_i32, [P(PlanT), P(Gateway), _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
                                          _f32, _f32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
         "tree_relay_add": (_i32, [_vp, _i32, _vp, _vp, _i32, _i32, _vp, _vp, _vp]),
+        "tree_gather_rows": (_i32, [_vp, _i32, _vp, _vp, _i32, _vp]),
         "tree_set_wait_limit_ns": (_i32, [_i64]),
         "tree_set_timing_events": (_i32, [ctypes.POINTER(_vp), _i32]),
         "tree_selftest_timeout": (_i32, [_vp, _i64, _vp]),
@@ -374,3 +375,17 @@ def tree_relay_add(rows, dk_gw, dv_gw, dk, dv, stream=None):
     _need(dv, tuple(dk.shape), torch.bfloat16, "dv")
     _check(_lib().tree_relay_add(_ptr(rows), A, _ptr(dk_gw), _ptr(dv_gw), Hkv, d, _ptr(dk), _ptr(dv),
                                  _stream(stream)), "tree_relay_add")
+
+
+def tree_gather_rows(rows, src, out=None, stream=None):
+    """out[r] = src[rows[r]] for bf16 src [M, ...]; rows int32 CUDA [n]."""
+    n = rows.shape[0]
+    _need(rows, (n,), torch.int32, "rows")
+    if not (src.is_cuda and src.is_contiguous() and src.dtype == torch.bfloat16):
+        raise ValueError("src: expected contiguous CUDA bf16")
+    row_elems = src[0].numel()
+    out = torch.empty((n,) + tuple(src.shape[1:]), dtype=src.dtype, device=src.device) if out is None else out
+    _need(out, (n,) + tuple(src.shape[1:]), torch.bfloat16, "out")
+    _check(_lib().tree_gather_rows(_ptr(rows), n, _ptr(src), _ptr(out), row_elems, _stream(stream)),
+           "tree_gather_rows")
+    return out

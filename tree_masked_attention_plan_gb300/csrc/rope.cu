@@ -77,6 +77,15 @@ __global__ void k_apply_weights(const float* __restrict__ w, const uint4* u, uin
   (void)row_vecs;
 }
 
+// dst[r] = src[rows[r]] for bf16 rows of row_elems elements (a multiple of 8), 16 bytes a thread
+__global__ void k_gather_rows(const int32_t* __restrict__ rows, int n, const uint4* __restrict__ src, uint4* dst,
+                              int row_vec) {
+  const size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= (size_t)n * row_vec) return;
+  const size_t r = e / row_vec, c = e % row_vec;
+  dst[e] = src[(size_t)rows[r] * row_vec + c];
+}
+
 }  // namespace
 }  // namespace ta
 
@@ -119,6 +128,20 @@ int tree_apply_weights(const tree_plan_t* plan, const tree_bf16* u, tree_bf16* d
   const size_t total = (size_t)plan->n_tokens * per_token;
   k_apply_weights<<<(unsigned)((total + 255) / 256), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
       plan->w, (const uint4*)u, (uint4*)dO, plan->n_tokens, per_token, per_token);
+  return record_cuda(cudaGetLastError());
+}
+
+int tree_gather_rows(const int32_t* rows, int32_t n, const tree_bf16* src, tree_bf16* dst, int row_elems,
+                     tree_stream_t stream) {
+  if (!rows || !src || !dst || n <= 0) return TREE_ERR_ARG;
+  if (row_elems <= 0 || row_elems % 8 != 0) return TREE_ERR_SHAPE;
+  if ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15) return TREE_ERR_ARG;
+  int rc = check_device();
+  if (rc) return rc;
+  const int row_vec = row_elems / 8;
+  const size_t total = (size_t)n * row_vec;
+  k_gather_rows<<<(unsigned)((total + 255) / 256), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      rows, n, reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), row_vec);
   return record_cuda(cudaGetLastError());
 }
 

@@ -1,0 +1,119 @@
+"""Host-side bookkeeping for running a tree as partitions ("Tree Training 技术详解", section 8.2).
+
+A tree too large for one pass is cut below a node `cut`: the parent partition keeps every node
+except the subtrees of cut's children, and each child of cut roots one child partition.  The
+child partitions read the K/V of the path root..cut (the gateway) from the parent partition
+instead of recomputing it, and their gradients w.r.t. the gateway are relayed back to it.
+
+This module only renumbers nodes and tokens (depth-first packing with children by ascending id,
+the same order the plan uses); the attention itself runs in the library.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+
+@dataclass
+class Partition:
+    parent: np.ndarray        # partition tree, node ids 0..n-1 (relative order of the whole tree's ids)
+    node_len: np.ndarray
+    nodes: np.ndarray         # whole-tree id of each partition node
+    tokens: np.ndarray        # whole-tree packed index of each partition token, in partition order
+    pos_offset: int           # first position of the partition's root(s): 0, or the gateway length
+
+
+def packed_starts(parent, node_len):
+    """First packed token of every node: depth-first preorder, roots and children by ascending id."""
+    parent = np.asarray(parent, dtype=np.int64)
+    node_len = np.asarray(node_len, dtype=np.int64)
+    kids = [[] for _ in range(len(parent))]
+    roots = []
+    for v, p in enumerate(parent):
+        (roots if p < 0 else kids[p]).append(v)
+    start = np.zeros(len(parent), dtype=np.int64)
+    tok = 0
+    for r in roots:
+        stack = [r]
+        while stack:
+            v = stack.pop()
+            start[v] = tok
+            tok += node_len[v]
+            stack.extend(reversed(kids[v]))       # ascending ids leave the stack in order
+    return start
+
+
+def _subtree(kids, v):
+    out, stack = [], [v]
+    while stack:
+        x = stack.pop()
+        out.append(x)
+        stack.extend(kids[x])
+    return out
+
+
+def _part(parent, node_len, starts, nodes, pos_offset):
+    nodes = np.array(sorted(nodes), dtype=np.int64)
+    remap = {int(v): i for i, v in enumerate(nodes)}
+    par = np.array([remap.get(int(parent[v]), -1) for v in nodes], dtype=np.int64)
+    lens = node_len[nodes]
+    sub = packed_starts(par, lens)
+    tokens = np.empty(int(lens.sum()), dtype=np.int64)
+    for i, v in enumerate(nodes):
+        tokens[sub[i]:sub[i] + lens[i]] = np.arange(starts[v], starts[v] + lens[i])
+    return Partition(parent=par, node_len=lens, nodes=nodes, tokens=tokens, pos_offset=pos_offset)
+
+
+def partition_tree(parent, node_len, cut: int) -> dict:
+    """Cut below node `cut` (which must have children).  Returns dict(parent=Partition,
+    children=[Partition], gw_tokens=whole-tree tokens of the path root..cut in path order,
+    gw_rows=their indices inside the parent partition, A=gateway length)."""
+    parent = np.asarray(parent, dtype=np.int64)
+    node_len = np.asarray(node_len, dtype=np.int64)
+    kids = [[] for _ in range(len(parent))]
+    for v, p in enumerate(parent):
+        if p >= 0:
+            kids[p].append(v)
+    if not kids[cut]:
+        raise ValueError(f"node {cut} has no children to cut off")
+    starts = packed_starts(parent, node_len)
+    path = [cut]
+    while parent[path[-1]] >= 0:
+        path.append(int(parent[path[-1]]))
+    path.reverse()
+    gw_tokens = np.concatenate([np.arange(starts[v], starts[v] + node_len[v]) for v in path]).astype(np.int64)
+    A = int(len(gw_tokens))
+    if A == 0:
+        raise ValueError("the path to the cut node holds no tokens")
+    child_sets = [_subtree(kids, c) for c in kids[cut]]
+    below = set(x for cs in child_sets for x in cs)
+    ppart = _part(parent, node_len, starts, [v for v in range(len(parent)) if v not in below], 0)
+    children = [_part(parent, node_len, starts, cs, A) for cs in child_sets if node_len[cs].sum() > 0]
+    where = np.empty(int(node_len.sum()), dtype=np.int64)
+    where[ppart.tokens] = np.arange(len(ppart.tokens))
+    return dict(parent=ppart, children=children, gw_tokens=gw_tokens, gw_rows=where[gw_tokens], A=A)
+
+
+def largest_cut(parent, node_len):
+    """A cut that moves the most tokens into child partitions: the node with children whose
+    children's subtrees hold the most tokens (ties: smallest id)."""
+    parent = np.asarray(parent, dtype=np.int64)
+    node_len = np.asarray(node_len, dtype=np.int64)
+    size = node_len.astype(np.int64).copy()
+    for v in sorted(range(len(parent)), key=lambda x: -_depth(parent, x)):
+        if parent[v] >= 0:
+            size[parent[v]] += size[v]
+    below = {}
+    for v, p in enumerate(parent):
+        if p >= 0:
+            below[p] = below.get(p, 0) + size[v]
+    return max(sorted(below), key=lambda v: below[v])
+
+
+def _depth(parent, v):
+    d = 0
+    while parent[v] >= 0:
+        v = parent[v]
+        d += 1
+    return d
