@@ -1,7 +1,8 @@
 // Tree-masked attention backward on tcgen05 ("Tree Training 技术详解", section 6.2 and
 // section 7: a shared ancestor's K/V receive the summed gradients of every descendant that
 // sees them).  Three kernels:
-//   k_bwd_pre      delta_i = sum_c dO_ic O_ic per (token, q head); zero the fp32 dQ accumulator.
+//   k_bwd_pre      delta_i = sum_c dO_ic O_ic per (token, q head), stored as -delta scale with
+//                  -LSE log2e beside it; k_zero_f32x4 zeroes the fp32 dQ accumulator.
 //   k_bwd_dkdv     one CTA per (key tile, kv head): loops over the q heads of the group and the
 //                  non-empty query tiles of the key tile's column.  Per step, in TMEM:
 //                    S^T  = K Q^T            (cols   0..127, lane = key)
@@ -103,31 +104,33 @@ DEVI void mbar_wait_drain_b(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
 }
 
 // ------------------------------------------------------------------------------------------
-// per query row: -delta scale (delta_i = sum_c dO_ic O_ic) and -LSE log2e; one group of HD/8
-// threads per (token, q head) row
+// per query row: -delta scale (delta_i = sum_c dO_ic O_ic) and -LSE log2e.  One block per
+// (32 tokens, q head): 8 threads per token each dot 16 columns (two 16-byte loads of O and of
+// dO, a 256-byte row per token), so the per-head outputs are written as coalesced 128-byte rows.
 template <int HD>
-__global__ void k_bwd_pre(const uint4* __restrict__ o, const uint4* __restrict__ dO, const float* __restrict__ lse,
-                          float* ndlt, float* nlse2, float scale, int N, int Npad, int Hq) {
-  constexpr int TPR = HD / 8;
-  const size_t gt = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const size_t row = gt / TPR;                  // row = token * Hq + h
-  const int sub = static_cast<int>(gt % TPR);
-  const size_t rows = (size_t)Npad * Hq;
+__global__ void __launch_bounds__(256) k_bwd_pre(const uint4* __restrict__ o, const uint4* __restrict__ dO,
+                                                 const float* __restrict__ lse, float* ndlt, float* nlse2, float scale,
+                                                 int N, int Npad, int Hq) {
+  constexpr int TPT = 8, VPT = HD / 8 / TPT;      // threads per token, 16-byte vectors per thread
+  const int h = blockIdx.y;
+  const int tok = blockIdx.x * 32 + threadIdx.x / TPT;
+  const int sub = threadIdx.x % TPT;
   float acc = 0.f;
-  const int tok = static_cast<int>(row / Hq);
-  if (row < rows && tok < N) {
-    const uint4 a = o[row * TPR + sub], b = dO[row * TPR + sub];
-    acc = bf16lo(a.x) * bf16lo(b.x) + bf16hi(a.x) * bf16hi(b.x) + bf16lo(a.y) * bf16lo(b.y) +
-          bf16hi(a.y) * bf16hi(b.y) + bf16lo(a.z) * bf16lo(b.z) + bf16hi(a.z) * bf16hi(b.z) +
-          bf16lo(a.w) * bf16lo(b.w) + bf16hi(a.w) * bf16hi(b.w);
+  if (tok < N) {
+    const size_t base = ((size_t)tok * Hq + h) * (HD / 8) + sub * VPT;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const uint4 a = o[base + v], b = dO[base + v];
+      acc += bf16lo(a.x) * bf16lo(b.x) + bf16hi(a.x) * bf16hi(b.x) + bf16lo(a.y) * bf16lo(b.y) +
+             bf16hi(a.y) * bf16hi(b.y) + bf16lo(a.z) * bf16lo(b.z) + bf16hi(a.z) * bf16hi(b.z) +
+             bf16lo(a.w) * bf16lo(b.w) + bf16hi(a.w) * bf16hi(b.w);
+    }
   }
 #pragma unroll
-  for (int off = TPR / 2; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (row < rows && sub == 0) {
-    // per query row constants of the elementwise pass, premultiplied once here
-    const int h = static_cast<int>(row % Hq);
+  for (int off = TPT / 2; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (sub == 0 && tok < Npad) {
     const size_t at = (size_t)h * Npad + tok;
-    ndlt[at] = -acc * scale;
+    ndlt[at] = tok < N ? -acc * scale : 0.f;
     nlse2[at] = -lse[at] * 1.4426950408889634f;
   }
 }
@@ -648,13 +651,15 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
 }
 
 // ------------------------------------------------------------------------------------------
-// dQ = R(pos)^T dQacc: one block per 32 tokens, all heads; angles computed once per token.
+// dQ = R(pos)^T dQacc: one block per (32 tokens, group of up to 8 q heads); angles computed
+// once per token and block.
 // Per head: the 32 rows of the [d/4][128][4] block are read with 16-byte loads (4 columns of
 // one row each; 32 threads cover 512 contiguous bytes), transposed through shared memory,
 // rotated, and written as 16-byte bf16 stores.
 template <int HD>
 __global__ void __launch_bounds__(256) k_dq_finalize(const float* __restrict__ dqacc, const int32_t* __restrict__ pos,
-                                                     __nv_bfloat16* dq, int N, int T, int Hq, float theta) {
+                                                     __nv_bfloat16* dq, int N, int T, int Hq, int heads_per_block,
+                                                     float theta) {
   constexpr int TT = 32, HALF = HD / 2, G = HALF / 8;   // G groups of 8 columns per half row
   __shared__ float s_cos[TT][HALF], s_sin[TT][HALF];
   __shared__ float tile[HD][TT + 1];
@@ -668,7 +673,8 @@ __global__ void __launch_bounds__(256) k_dq_finalize(const float* __restrict__ d
     s_sin[t][c] = sv;
   }
   const int t_out = threadIdx.x / G, g_out = threadIdx.x % G;
-  for (int h = 0; h < Hq; ++h) {
+  const int h0 = blockIdx.y * heads_per_block;
+  for (int h = h0; h < h0 + heads_per_block; ++h) {
     __syncthreads();
     const float* src = dqacc + ((size_t)h * T + i0 / TILE) * HD * TILE + 4 * (i0 % TILE);
     for (int e = threadIdx.x; e < (HD / 4) * TT; e += blockDim.x) {
@@ -741,8 +747,7 @@ int launch_bwd(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k, 
   }
   record_timing_event(0, s);
   {
-    const size_t threads = (size_t)Npad * Hq * (HD / 8);
-    k_bwd_pre<HD><<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(
+    k_bwd_pre<HD><<<dim3(Npad / 32, Hq), 256, 0, s>>>(
         reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dO), lse, ndlt, nlse2, scale, N, Npad, Hq);
     const size_t n4 = (size_t)Hq * HD * Npad / 4;
     k_zero_f32x4<<<(unsigned)std::min<size_t>((n4 + 255) / 256, 152 * 16), 256, 0, s>>>(
@@ -755,8 +760,13 @@ int launch_bwd(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k, 
   record_timing_event(1, s);
   k_bwd_dkdv<HD><<<(T + G) * Hkv, C::THREADS, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, tkg, tvg, P);
   record_timing_event(2, s);
-  k_dq_finalize<HD><<<(N + 31) / 32, 256, 0, s>>>(dqacc, plan->pos, reinterpret_cast<__nv_bfloat16*>(dq), N, T, Hq,
-                                                  theta);
+  {
+    int hpb = 1;                                  // heads per block: the largest divisor of Hq up to 8
+    for (int c = 8; c > 1; --c)
+      if (Hq % c == 0) { hpb = c; break; }
+    k_dq_finalize<HD><<<dim3((N + 31) / 32, Hq / hpb), 256, 0, s>>>(
+        dqacc, plan->pos, reinterpret_cast<__nv_bfloat16*>(dq), N, T, Hq, hpb, theta);
+  }
   record_timing_event(3, s);
   return record_cuda(cudaGetLastError());
 }
