@@ -4,6 +4,9 @@
   element by element with the oracle's per-node form (heads computed in a spawn pool);
 * forest / large128k (~131K tokens): exact oracle results on sampled query nodes (leaves and
   a root), whose rows (O, LSE, dQ) and own keys (dK, dV of leaves) the oracle computes alone;
+* rollout32k run as gateway partitions (cut below the node whose children's subtrees hold the
+  most tokens, the launch configuration of `bench.py --partition`): the same kv-head group
+  against the same oracle results;
 * all three: identities that hold at any size and cover every gradient entry in aggregate:
   sum_j dV_j = sum_i sum_{h in group} dO_i (softmax rows sum to one) and, for gradients
   w.r.t. the rotated keys, sum_j dK_j = 0 (every row of dS sums to zero)."""
@@ -20,6 +23,7 @@ from _gpu import GRAD_TOL, O_TOL, f64, oracle_heads_parallel, run_gpu
 pytestmark = pytest.mark.gpu
 
 _CACHE = {}
+_REFS = {}
 
 
 def _gpu(name):
@@ -54,7 +58,7 @@ def _cmp(name, heads, refs, rows):
 def test_rollout32k_whole_kv_group():
     heads = [0, 1, 2, 3]
     _gpu("rollout32k")
-    refs = oracle_heads_parallel("rollout32k", heads)
+    refs = _REFS.setdefault("rollout32k", oracle_heads_parallel("rollout32k", heads))
     e = _cmp("rollout32k", heads, refs, None)
     print("rollout32k kv group 0:", e)
     assert e["o"] <= O_TOL and e["lse"] <= O_TOL
@@ -96,3 +100,59 @@ def test_gradient_identities(name):
     print(f"{name}: sum dV identity rel err {err_v:.2e}; |sum dK| / sum|dK| {err_k:.2e}")
     assert err_v <= 2e-2
     assert err_k <= 2e-2
+
+
+def _run_partitioned(wl, t, dev):
+    """Parent partition, then every child partition below the gateway, then the relay; outputs
+    scattered back to the whole tree's token order."""
+    from tree_masked_attention_plan_gb300.partition import largest_cut, partition_tree
+    P = partition_tree(wl.parent, wl.node_len, largest_cut(wl.parent, wl.node_len))
+    N, Hq, Hkv, d, th = wl.n_tokens, wl.Hq, wl.Hkv, wl.d, wl.theta
+    st = tam.new_status(dev)
+    full = tam.tree_plan(wl.parent, wl.node_len, device=dev)
+    dO_full = tam.tree_apply_weights(full, t["u"].to(dev))
+    out = {x: torch.zeros(N, H, d, dtype=torch.bfloat16, device=dev)
+           for x, H in (("o", Hq), ("dq", Hq), ("dk", Hkv), ("dv", Hkv))}
+    lse = torch.zeros(Hq, N, dtype=torch.float32, device=dev)
+    res = []
+    for part in [P["parent"]] + P["children"]:
+        idx = torch.as_tensor(part.tokens, device=dev)
+        q, k, v = (t[x].to(dev)[idx].contiguous() for x in ("q", "k", "v"))
+        pl = tam.tree_plan(part.parent, part.node_len, device=dev, pos_offset=part.pos_offset)
+        qr, kr = tam.tree_rope_fwd(pl, q, k, th)
+        res.append((part, idx, pl, qr, kr, v, dO_full[idx].contiguous()))
+    part, idx, pl, qr, kr, v, dO = res[0]
+    o, l = tam.tree_attn_fwd(pl, qr, kr, v, status=st)
+    rows = torch.as_tensor(P["gw_rows"], dtype=torch.int32, device=dev)
+    k_gw, v_gw = tam.tree_gather_rows(rows, kr), tam.tree_gather_rows(rows, v)
+    dq, dk, dv = tam.tree_attn_bwd(pl, qr, kr, v, o, l, dO, rope_theta=th, status=st)
+    dk_gw = torch.zeros(P["A"], Hkv, d, dtype=torch.float32, device=dev)
+    dv_gw = torch.zeros_like(dk_gw)
+    for part_c, idx_c, pl_c, qr_c, kr_c, v_c, dO_c in res[1:]:
+        o_c, l_c = tam.tree_attn_fwd_gateway(pl_c, k_gw, v_gw, qr_c, kr_c, v_c, status=st)
+        dq_c, dk_c, dv_c = tam.tree_attn_bwd_gateway(pl_c, k_gw, v_gw, qr_c, kr_c, v_c, o_c, l_c, dO_c, dk_gw, dv_gw,
+                                                     rope_theta=th, status=st)
+        out["o"][idx_c], out["dq"][idx_c], out["dk"][idx_c], out["dv"][idx_c] = o_c, dq_c, dk_c, dv_c
+        lse[:, idx_c] = l_c[:, :len(idx_c)]
+    tam.tree_relay_add(rows, dk_gw, dv_gw, dk, dv)
+    out["o"][idx], out["dq"][idx], out["dk"][idx], out["dv"][idx] = o, dq, dk, dv
+    lse[:, idx] = l[:, :len(idx)]
+    torch.cuda.synchronize()
+    tam.check_status(st, "partitioned rollout32k")
+    out["lse"] = lse
+    return P, out
+
+
+def test_rollout32k_as_gateway_partitions():
+    heads = [0, 1, 2, 3]
+    wl = make_workload("rollout32k")
+    t = make_tensors(wl)
+    _CACHE.clear()
+    P, g = _run_partitioned(wl, t, torch.device("cuda", 0))
+    _CACHE["rollout32k"] = (wl, t, g)
+    refs = _REFS.setdefault("rollout32k", oracle_heads_parallel("rollout32k", heads))
+    e = _cmp("rollout32k", heads, refs, None)
+    print(f"rollout32k as partitions (gateway {P['A']} tokens, children "
+          f"{[len(c.tokens) for c in P['children']]}), kv group 0:", e)
+    assert e["o"] <= O_TOL and e["lse"] <= O_TOL
+    assert max(e["dq"], e["dk"], e["dv"]) <= GRAD_TOL
