@@ -35,8 +35,9 @@ METRIC = "tree-attn fwd+bwd visible-pair TFLOP/s and tokens/s on 1 GB300; % of b
 UNIT = "TFLOP/s"
 DEFAULT_CONFIG = "rollout32k"
 # kernels of this library per step: plan (expand, zero, hi range, node runs, rows, cols, scan and
-# orders, fill), RoPE, forward, loss weights, backward (delta, zero dQ accumulator, dK/dV, dQ)
-LAUNCHES_PER_STEP = 8 + 1 + 1 + 1 + 4
+# orders, fill), RoPE, forward, loss weights, backward (delta and dQ-accumulator zeroing, dK/dV,
+# dQ finalize)
+LAUNCHES_PER_STEP = 8 + 1 + 1 + 1 + 3
 DKDV_PROFILE = os.path.join(ROOT, "profiles", "k_bwd_dkdv_rollout32k.md")
 DKDV_SOURCES = [os.path.join(ROOT, "tree_masked_attention_plan_gb300", "csrc", f) for f in ("attn_bwd.cu", "common.cuh")]
 
@@ -342,7 +343,7 @@ def run_partitioned(args, dev):
     info = dict(cut_node=int(cut), gateway_tokens=A, parent_tokens=int(len(P["parent"].tokens)),
                 child_tokens=[int(len(c.tokens)) for c in P["children"]])
     return dict(st=st, wl=wl, ms=float(np.mean(ms)), clocks=clk.summary(), info=info,
-                launches=LAUNCHES_PER_STEP - 1 + 14 * len(P["children"]) + 3)
+                launches=(LAUNCHES_PER_STEP - 1) * (1 + len(P["children"])) + 3)
 
 
 def cpu_baseline_sample(config, budget_s=20.0):

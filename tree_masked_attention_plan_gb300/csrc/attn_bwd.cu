@@ -2,7 +2,7 @@
 // section 7: a shared ancestor's K/V receive the summed gradients of every descendant that
 // sees them).  Three kernels:
 //   k_bwd_pre      delta_i = sum_c dO_ic O_ic per (token, q head), stored as -delta scale with
-//                  -LSE log2e beside it; k_zero_f32x4 zeroes the fp32 dQ accumulator.
+//                  -LSE log2e beside it; zeroes the fp32 dQ accumulator on the way.
 //   k_bwd_dkdv     one CTA per (key tile, kv head): loops over the q heads of the group and the
 //                  non-empty query tiles of the key tile's column.  Per step, in TMEM:
 //                    S^T  = K Q^T            (cols   0..127, lane = key)
@@ -104,13 +104,14 @@ DEVI void mbar_wait_drain_b(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
 }
 
 // ------------------------------------------------------------------------------------------
-// per query row: -delta scale (delta_i = sum_c dO_ic O_ic) and -LSE log2e.  One block per
-// (32 tokens, q head): 8 threads per token each dot 16 columns (two 16-byte loads of O and of
-// dO, a 256-byte row per token), so the per-head outputs are written as coalesced 128-byte rows.
+// per query row: -delta scale (delta_i = sum_c dO_ic O_ic) and -LSE log2e, and zeroes of the
+// same rows of the dQ accumulator.  One block per (32 tokens, q head): 8 threads per token
+// each dot 16 columns (two 16-byte loads of O and of dO, a 256-byte row per token), so the
+// per-head outputs are written as coalesced 128-byte rows.
 template <int HD>
 __global__ void __launch_bounds__(256) k_bwd_pre(const uint4* __restrict__ o, const uint4* __restrict__ dO,
                                                  const float* __restrict__ lse, float* ndlt, float* nlse2, float scale,
-                                                 int N, int Npad, int Hq) {
+                                                 float* dqacc, int N, int Npad, int Hq) {
   constexpr int TPT = 8, VPT = HD / 8 / TPT;      // threads per token, 16-byte vectors per thread
   const int h = blockIdx.y;
   const int tok = blockIdx.x * 32 + threadIdx.x / TPT;
@@ -133,11 +134,12 @@ __global__ void __launch_bounds__(256) k_bwd_pre(const uint4* __restrict__ o, co
     ndlt[at] = tok < N ? -acc * scale : 0.f;
     nlse2[at] = -lse[at] * 1.4426950408889634f;
   }
-}
-
-__global__ void k_zero_f32x4(float4* p, size_t n4) {
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x)
-    p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  // dQ accumulator rows of these 32 tokens for head h: [HD/4][128][4] block of (h, query tile),
+  // 32 consecutive rows = 512 contiguous bytes per 4 columns
+  const int t0 = blockIdx.x * 32;
+  float4* blk = reinterpret_cast<float4*>(dqacc + ((size_t)h * (Npad / TILE) + t0 / TILE) * HD * TILE) + (t0 % TILE);
+  for (int e = threadIdx.x; e < (HD / 4) * 32; e += blockDim.x)
+    blk[(size_t)(e / 32) * TILE + (e % 32)] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -748,10 +750,8 @@ int launch_bwd(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k, 
   record_timing_event(0, s);
   {
     k_bwd_pre<HD><<<dim3(Npad / 32, Hq), 256, 0, s>>>(
-        reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dO), lse, ndlt, nlse2, scale, N, Npad, Hq);
-    const size_t n4 = (size_t)Hq * HD * Npad / 4;
-    k_zero_f32x4<<<(unsigned)std::min<size_t>((n4 + 255) / 256, 152 * 16), 256, 0, s>>>(
-        reinterpret_cast<float4*>(dqacc), n4);
+        reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dO), lse, ndlt, nlse2, scale, dqacc, N, Npad,
+        Hq);
   }
   BwdParams P{plan->col_ptr, plan->col_idx, plan->col_order, plan->tok_in, plan->tok_out, plan->pos,
               plan->tile_runs, plan->tile_nruns, plan->tile_class, nlse2, ndlt, dqacc, reinterpret_cast<__nv_bfloat16*>(dk),
