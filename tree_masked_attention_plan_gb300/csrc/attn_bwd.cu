@@ -42,15 +42,17 @@ struct BwdCfg {
   static constexpr int AUX_LSE = 0, AUX_DLT = TILE * 4, AUX_QIN = 2 * TILE * 4, AUX_RUNS = 3 * TILE * 4;
   static constexpr int AUX_BYTES = AUX_RUNS + TREE_MAX_RUNS * 16;
   static constexpr int AUX_OFF = DST_OFF + 2 * CHUNK_BYTES;    // two stages
-  static constexpr int STG_OFF = AUX_OFF + 2 * AUX_BYTES;      // dQ staging: 2 x [4][128][4] fp32
+  static constexpr int NSTG = 3;                                // dQ staging buffers in flight
+  static constexpr int STG_OFF = AUX_OFF + 2 * AUX_BYTES;      // dQ staging: NSTG x [4][128][4] fp32
   static constexpr int STG_BYTES = 16 * TILE * 4;
-  static constexpr int LIST_OFF = STG_OFF + 2 * STG_BYTES;     // int32 query tiles of the column
+  static constexpr int LIST_OFF = STG_OFF + NSTG * STG_BYTES;  // int32 query tiles of the column
   static constexpr int LCLS_OFF = LIST_OFF + kMaxList * 4;     // uint8 their tile classes
   static constexpr int BAR_OFF = LCLS_OFF + kMaxList;
   static constexpr int NBAR = 15;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int SMEM = MISC_OFF + 16;
   static constexpr int SMEM_ALLOC = SMEM + 1024;
+  static_assert(SMEM_ALLOC <= 232448, "dynamic shared memory above the 227 KB a CTA may use");
   // 16 warps = 4 warpgroups: [producer, MMA, 2 idle] [4 dQ drain] [4 + 4 elementwise]
   static constexpr int THREADS = 512;
   static constexpr int LAUNCH_REGS = 128;                      // 512 x 128 = the whole register file
@@ -362,7 +364,7 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
     // ---------------------------------------------------------------- dQ drain warpgroup
     // Thread r copies dQ(n) row r (all HD columns) out of TMEM and frees the columns for
     // dP(n+1).  The rows then go to the fp32 accumulator 16 columns (8 KiB) at a time through a
-    // double-buffered shared staging area and a bulk reduce-add by the TMA unit, while the next
+    // three-buffer shared staging ring and a bulk reduce-add by the TMA unit, while the next
     // step runs: no per-element atomics compete with the tensor-core issue for the memory pipe.
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
@@ -370,6 +372,7 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
     float* stg = reinterpret_cast<float*>(sm + C::STG_OFF);
     const bool leader = (threadIdx.x == 128);
     int groups = 0;                               // bulk groups committed by the leader
+    int stage_slot = 0;                           // next staging buffer (same on every drain thread)
     for (int n = 0; n < total; ++n) {
       int h, qt, cls;
       step_tile(n, h, qt, cls);
@@ -389,8 +392,12 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
       float* blk = p.dqacc + ((size_t)h * p.T + qt) * HD * TILE;
 #pragma unroll
       for (int gi = 0; gi < HD / 16; ++gi) {
-        float* buf = stg + (gi & 1) * (C::STG_BYTES / 4);
-        if (leader && groups >= 2) bulk_wait_group_read1();   // the reduce that last read `buf` is done
+        // staging buffer of the drain's running group count: the reduce that last read it is
+        // the third-newest, so two reduces stay queued for the TMA unit while this one is filled
+        const int slot = stage_slot;
+        stage_slot = (stage_slot + 1 == C::NSTG) ? 0 : stage_slot + 1;
+        float* buf = stg + slot * (C::STG_BYTES / 4);
+        if (leader && groups >= C::NSTG) bulk_wait_group_read2();
         named_bar_sync(1, 128);
 #pragma unroll
         for (int j = 0; j < 4; ++j)

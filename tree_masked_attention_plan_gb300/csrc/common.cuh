@@ -160,6 +160,8 @@ DEVI void bulk_reduce_add_f32(float* gdst, const void* ssrc, uint32_t bytes) {
 DEVI void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // wait until the shared-memory sources of every committed bulk group but the newest have been read
 DEVI void bulk_wait_group_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+// ... all but the two newest
+DEVI void bulk_wait_group_read2() { asm volatile("cp.async.bulk.wait_group.read 2;" ::: "memory"); }
 // wait until every committed bulk group has completed (its global writes performed)
 DEVI void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 DEVI void named_bar_sync(int id, int count) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory"); }
