@@ -346,6 +346,130 @@ def run_partitioned(args, dev):
                 launches=(LAUNCHES_PER_STEP - 1) * (1 + len(P["children"])) + 3)
 
 
+CONV_METRIC = "tree causal conv1d fwd+bwd algorithmic GB/s on 1 GB300 (hybrid-layer context, section 9.2)"
+
+
+def run_conv(args, dev):
+    """Hybrid-layer depthwise causal convolution along root paths (Tree Training explainer,
+    section 9.2), forward and backward with bias, on the workload's tree: x, dy [N, C] bf16, taps
+    [K, C] fp32.  Algorithmic bytes: forward reads x and writes y (4 B per element), backward
+    reads x and dy and writes dx (6 B per element); the taps and dw are negligible."""
+    import tree_masked_attention_plan_gb300 as tam
+    from workloads import make_conv_tensors
+    torch.cuda.set_device(dev)
+    wl = make_workload(args.config)
+    C, K = args.conv_channels, args.conv_k
+    plan = tam.tree_plan(wl.parent, wl.node_len, device=dev)
+    N = plan.n_tokens
+    tree = tam.tree_arrays(wl.parent, wl.node_len, dev)
+    t = make_conv_tensors(N, C, K, seed=11)
+    x, w, b, dy = t["x"].to(dev), t["w"].to(dev), t["bias"].to(dev), t["u"].to(dev)
+    y = torch.empty_like(x)
+    ws = torch.empty(tam.tree_conv1d_bwd_workspace(plan, C), dtype=torch.uint8, device=dev)
+    dx, dw, db = torch.empty_like(x), torch.empty_like(w), torch.empty_like(b)
+    lib = tam._lib()
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+
+    status = tam.new_status(dev)
+    st = status.data_ptr()
+
+    def step():
+        tam._check(lib.tree_conv1d_fwd(plan.ref(), tree[0].data_ptr(), tree[1].data_ptr(), x.data_ptr(), w.data_ptr(),
+                                       b.data_ptr(), C, K, y.data_ptr(), st, sp), "conv fwd")
+        ev[1].record(stream)
+        tam._check(lib.tree_conv1d_bwd(plan.ref(), tree[0].data_ptr(), tree[1].data_ptr(), x.data_ptr(), w.data_ptr(),
+                                       dy.data_ptr(), C, K, ws.data_ptr(), dx.data_ptr(), dw.data_ptr(),
+                                       db.data_ptr(), st, sp), "conv bwd")
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    fwd, bwd, tot = [], [], []
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        for _ in range(args.steps):
+            flush.fill_(1.0)
+            ev[0].record(stream)
+            step()
+            ev[2].record(stream)
+            torch.cuda.synchronize()
+            fwd.append(ev[0].elapsed_time(ev[1]))
+            bwd.append(ev[1].elapsed_time(ev[2]))
+            tot.append(ev[0].elapsed_time(ev[2]))
+    clocks = clk.summary()
+    tam.check_status(status, "conv steps")
+    # end to end through the public binding: pinned host x, dy in; dx, dw, db out, every step
+    hx, hdy = t["x"].pin_memory(), t["u"].pin_memory()
+    hdx = torch.empty(N, C, dtype=torch.bfloat16).pin_memory()
+    hdw, hdb = torch.empty(K, C).pin_memory(), torch.empty(C).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e = []
+    for i in range(args.warmup + args.steps):
+        flush.fill_(1.0)
+        e0.record(stream)
+        x.copy_(hx, non_blocking=True)
+        dy.copy_(hdy, non_blocking=True)
+        step()
+        hdx.copy_(dx, non_blocking=True)
+        hdw.copy_(dw, non_blocking=True)
+        hdb.copy_(db, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            e2e.append(e0.elapsed_time(e1))
+    ms_f, ms_b, ms = (float(np.mean(v)) for v in (fwd, bwd, tot))
+    elems = N * C
+    algo = 10.0 * elems
+    peaks = load_peaks()
+    achieved_b = 6.0 * elems / (ms_b * 1e-3) / 1e9
+    line = {
+        "metric": CONV_METRIC, "value": round(algo / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in/out, fp32 accumulate",
+        "data": "synthetic (seeded tree, N(0,1) bf16 x and dy, N(0,1/K) taps)",
+        "config": {"workload": f"{wl.name} conv C={C} K={K}", "N": N, "C": C, "K": K, "n_nodes": len(wl.parent),
+                   "step": "tree_conv1d_fwd + tree_conv1d_bwd (bias, dw, db)",
+                   "l2": "inputs (N C bf16) larger than L2, and flushed between steps"},
+        "breakdown_ms": {"fwd": round(ms_f, 4), "bwd": round(ms_b, 4),
+                         "fwd_gbs": round(4.0 * elems / (ms_f * 1e-3) / 1e9, 1)},
+        "roofline": {"kernel": "tree_conv1d_bwd (zero, k_conv_bwd, finish)", "bound": "hbm",
+                     "achieved": round(achieved_b, 1), "peak": peaks["hbm"], "unit": "GB/s",
+                     "frac": round(achieved_b / peaks["hbm"], 4), "peak_source": f"{peaks['source']} copy bandwidth",
+                     "traffic": None, "algorithmic": "6 B per element (read x, dy; write dx)"},
+        "e2e": {"value": round(algo / (float(np.mean(e2e)) * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "ms_per_step": round(float(np.mean(e2e)), 4), "h2d_bytes_per_step": 2 * elems * 2,
+                "d2h_bytes_per_step": elems * 2 + (K + 1) * C * 4},
+        "gpu_launches": 4 * args.steps, "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = conv_cpu_baseline(wl, t, budget_s=15.0)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def conv_cpu_baseline(wl, t, budget_s=15.0):
+    """The oracle's path-expanded fp64 convolution (forward and gradients) on a channel sample,
+    growing the sample until the time budget is spent; credited 10 B per element like the GPU."""
+    import oracle
+    p = oracle.plan(wl.parent, wl.node_len)
+    x, w, b, u = (t[n] for n in ("x", "w", "bias", "u"))
+    done, t0, c0 = 0, time.perf_counter(), 0
+    while time.perf_counter() - t0 < budget_s and c0 < x.shape[1]:
+        ch = slice(c0, c0 + 8)
+        f64 = [a[..., ch].double().numpy() for a in (x, w, b, u)]
+        oracle.conv_paths(wl.parent, wl.node_len, *f64, p=p)
+        done += x.shape[0] * 8
+        c0 += 8
+    el = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return dict(value=round(10.0 * done / el / 1e9, 4), unit="GB/s", cores=cores, kind="oracle",
+                sample=f"{wl.name}: fp64 path-expanded conv fwd+grads on channels 0-{c0 - 1} of {x.shape[1]}, "
+                       f"{el:.1f} s; NumPy default threads")
+
+
 def cpu_baseline_sample(config, budget_s=20.0):
     """The oracle as it stands, on the host cores: path-expanded fp64 attention fwd+bwd for q head 0
     over a prefix of the root-to-leaf paths that fits the time budget.  Credit: 14 d times the
@@ -382,6 +506,10 @@ def main():
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=list(CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--conv", action="store_true",
+                    help="time the hybrid-layer tree convolution (forward + backward) instead of attention")
+    ap.add_argument("--conv-channels", type=int, default=8192)
+    ap.add_argument("--conv-k", type=int, default=4)
     ap.add_argument("--partition", action="store_true",
                     help="run the tree as gateway partitions (parent + children of the largest cut)")
     args = ap.parse_args()
@@ -398,6 +526,10 @@ def main():
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local)
+    if args.conv:
+        if world > 1:
+            raise SystemExit("--conv runs on one GPU")
+        return run_conv(args, dev)
     if args.partition:
         res = run_partitioned(args, dev)
         ms_max, = reduce_max([res["ms"]], dev, world)

@@ -262,6 +262,51 @@ int tree_attn_bwd_noalloc(const tree_plan_t* plan, const tree_bf16* q, const tre
                           int32_t* status_dev, tree_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
+ * Hybrid layers over the packed tree ("Tree Training 技术详解", section 9).  In depth-first packing the
+ * token before a node's first token belongs to the previous node in preorder, not to the
+ * node's parent; layers that carry context along the sequence must take it from the parent.
+ * parent, node_len: the tree as given to tree_plan, as device int32 arrays [n_nodes].
+ * -------------------------------------------------------------------------------------*/
+
+/* Causal depthwise convolution along root paths (section 9.2):
+ *   y[t][c] = bias[c] + sum_{k < K} w[k][c] * x[prev_k(t)][c],
+ * prev_0(t) = t and prev_k(t) the token k steps before t on its root path: earlier tokens of
+ * t's node, then the last tokens of its parent (the nearest ancestor holding tokens), and so
+ * on; terms before the root are zero.  Every token gets what a causal convolution over any
+ * root-to-leaf path through it gives.  x, y [N][C] bf16 in packed order; w [K][C] fp32; bias
+ * [C] fp32 or NULL.  C a multiple of 8, 1 <= K <= 8 (else TREE_ERR_SHAPE); pointers 16-byte
+ * aligned (else TREE_ERR_ARG).  status_dev (device int32, may be NULL) receives
+ * TREE_ERR_TIMEOUT if a wait for a staged tile runs past the wait limit, as for tree_attn_fwd. */
+int tree_conv1d_fwd(const tree_plan_t* plan, const int32_t* parent, const int32_t* node_len,
+                    const tree_bf16* x, const float* w, const float* bias, int C, int K,
+                    tree_bf16* y, int32_t* status_dev, tree_stream_t stream);
+
+/* Bytes of workspace tree_conv1d_bwd needs: an fp32 [N][C] array of which it uses only the
+ * last K-1 rows of each node (the rows that also receive terms from the node's descendants). */
+size_t tree_conv1d_bwd_workspace(const tree_plan_t* plan, int C);
+
+/* Backward of tree_conv1d_fwd for an upstream gradient dy [N][C] bf16: dx [N][C] bf16 (each
+ * x[j] collects w[k] dy[t] from every t with prev_k(t) = j: a node's last tokens feed all its
+ * children), dw [K][C] and, if dbias is not NULL, dbias [C] fp32 (overwritten).  A dx row
+ * inside a node gathers its K terms in a fixed order (deterministic); the last K-1 rows of a
+ * node, dw and dbias are fp32 atomic sums, whose rounding order (not value) varies between runs.
+ * Same shape and pointer rules as tree_conv1d_fwd; the workspace 16-byte aligned. */
+int tree_conv1d_bwd(const tree_plan_t* plan, const int32_t* parent, const int32_t* node_len,
+                    const tree_bf16* x, const float* w, const tree_bf16* dy, int C, int K,
+                    void* workspace, tree_bf16* dx, float* dw, float* dbias, int32_t* status_dev,
+                    tree_stream_t stream);
+
+/* Recurrent-state routing (section 9.1): init[v] = final[a(v)], a(v) the nearest ancestor of
+ * node v that holds tokens (zeros for roots), fp32 [n_nodes][S], S a multiple of 4. */
+int tree_route_states(const int32_t* parent, const int32_t* node_len, int32_t n_nodes,
+                      const float* final_states, int S, float* init_states, tree_stream_t stream);
+
+/* Its backward: d_final[a(v)] += d_init[v] for every node v with such an ancestor (a parent
+ * receives the sum over its children); d_final is accumulated into, not overwritten. */
+int tree_route_states_bwd(const int32_t* parent, const int32_t* node_len, int32_t n_nodes,
+                          const float* d_init, int S, float* d_final, tree_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
  * Diagnostics
  * -------------------------------------------------------------------------------------*/
 

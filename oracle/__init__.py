@@ -16,6 +16,8 @@ Modules
 ``attention``  fp64 RoPE, path-expanded causal attention forward+backward (the
                definition), the per-node tree-mask formulation used for large trees,
                and the associative (max, numerator, denominator) softmax merge.
+``hybrid``     section 9: the path-expanded causal convolution (forward and backward)
+               and the parent-routed recurrent state with its transpose.
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py`` against the
 pages' worked example, closed forms, brute force on tiny inputs, library routines in
@@ -25,7 +27,9 @@ from .tree import (TreeError, validate_tree, root_to_leaf_paths, plan, tile_clas
                    tree_stats, TILE)
 from .attention import (rope, rope_transpose, attention_paths, attention_nodes,
                         merge_softmax_state, softmax_state)
+from .hybrid import conv_paths, route_states, route_states_bwd
 
 __all__ = ["TreeError", "validate_tree", "root_to_leaf_paths", "plan", "tile_classes",
            "tree_stats", "TILE", "rope", "rope_transpose", "attention_paths",
-           "attention_nodes", "merge_softmax_state", "softmax_state"]
+           "attention_nodes", "merge_softmax_state", "softmax_state", "conv_paths",
+           "route_states", "route_states_bwd"]

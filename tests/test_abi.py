@@ -121,3 +121,22 @@ def test_gateway_entry_points_reject_bad_arguments_without_a_gpu(lib):
     assert lib.tree_plan_offset(par.ctypes.data, ln.ctypes.data, 2, -1, plan, None) == -6
     assert lib.tree_attn_fwd_gateway(None, None, None, None, None, 1, 1, 64, ctypes.c_float(0.0), None, None,
                                      None, None) != 0
+
+
+def test_hybrid_entry_points_reject_bad_arguments_without_a_gpu(lib):
+    """Shape and pointer checks of the hybrid-layer entry points run before any CUDA call."""
+    f = lib.tree_route_states
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                  ctypes.c_void_p]
+    buf = ctypes.create_string_buffer(4096)
+    a = ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 16
+    assert f(a, a, 4, a, 6, a, None) == -2                      # S not a multiple of 4: TREE_ERR_SHAPE
+    assert f(None, a, 4, a, 8, a, None) == -6                   # NULL: TREE_ERR_ARG
+    assert f(a, a, 4, a + 4, 8, a, None) == -6                  # misaligned
+    g = lib.tree_route_states_bwd
+    g.restype = ctypes.c_int
+    g.argtypes = f.argtypes
+    assert g(a, a, 0, a, 8, a, None) == -6
+    assert lib.tree_conv1d_fwd(None, None, None, None, None, None, 8, 4, None, None, None) != 0
+    assert lib.tree_conv1d_bwd_workspace(None, 8) == 0

@@ -7,7 +7,8 @@ functions carry the C entry points' names (``include/tree_attn.h``):
 
   tree_plan_query, tree_plan (pos_offset -> tree_plan_offset), tree_rope_fwd,
   tree_apply_weights, tree_attn_fwd, tree_attn_bwd_workspace, tree_attn_bwd,
-  tree_attn_fwd_gateway, tree_attn_bwd_gateway, tree_relay_add, tree_gather_rows, tree_selftest_timeout,
+  tree_attn_fwd_gateway, tree_attn_bwd_gateway, tree_relay_add, tree_gather_rows, tree_conv1d_fwd,
+  tree_conv1d_bwd_workspace, tree_conv1d_bwd, tree_route_states, tree_route_states_bwd, tree_selftest_timeout,
   tree_set_wait_limit_ns
 
 Semantics follow "Tree Training 技术详解" (tingdeliu.github.io): DFS packing (section 3.2),
@@ -97,6 +98,11 @@ def _lib():
                                          _f32, _f32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
         "tree_relay_add": (_i32, [_vp, _i32, _vp, _vp, _i32, _i32, _vp, _vp, _vp]),
         "tree_gather_rows": (_i32, [_vp, _i32, _vp, _vp, _i32, _vp]),
+        "tree_conv1d_fwd": (_i32, [P(PlanT), _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp]),
+        "tree_conv1d_bwd_workspace": (ctypes.c_size_t, [P(PlanT), _i32]),
+        "tree_conv1d_bwd": (_i32, [P(PlanT), _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp]),
+        "tree_route_states": (_i32, [_vp, _vp, _i32, _vp, _i32, _vp, _vp]),
+        "tree_route_states_bwd": (_i32, [_vp, _vp, _i32, _vp, _i32, _vp, _vp]),
         "tree_set_wait_limit_ns": (_i32, [_i64]),
         "tree_set_timing_events": (_i32, [ctypes.POINTER(_vp), _i32]),
         "tree_selftest_timeout": (_i32, [_vp, _i64, _vp]),
@@ -389,3 +395,69 @@ def tree_gather_rows(rows, src, out=None, stream=None):
     _check(_lib().tree_gather_rows(_ptr(rows), n, _ptr(src), _ptr(out), row_elems, _stream(stream)),
            "tree_gather_rows")
     return out
+
+
+def tree_arrays(parent, node_len, device):
+    """The tree as device int32 arrays (parent, node_len), as the hybrid-layer entry points take it."""
+    return (torch.as_tensor(_host_i32(parent), device=device), torch.as_tensor(_host_i32(node_len), device=device))
+
+
+def tree_conv1d_fwd(plan: TreePlan, tree, x, w, bias=None, out=None, status=None, stream=None):
+    """Causal depthwise convolution along root paths: x [N, C] bf16, w [K, C] fp32, bias [C] fp32."""
+    parent, node_len = tree
+    N, C = x.shape
+    K = w.shape[0]
+    _need(x, (plan.n_tokens, C), torch.bfloat16, "x")
+    _need(w, (K, C), torch.float32, "w")
+    if bias is not None:
+        _need(bias, (C,), torch.float32, "bias")
+    out = torch.empty_like(x) if out is None else out
+    _check(_lib().tree_conv1d_fwd(plan.ref(), _ptr(parent), _ptr(node_len), _ptr(x), _ptr(w), _ptr(bias), C, K,
+                                  _ptr(out), _ptr(status), _stream(stream)), "tree_conv1d_fwd")
+    return out
+
+
+def tree_conv1d_bwd_workspace(plan: TreePlan, C):
+    """Bytes of workspace tree_conv1d_bwd needs for C channels."""
+    return int(_lib().tree_conv1d_bwd_workspace(plan.ref(), C))
+
+
+def tree_conv1d_bwd(plan: TreePlan, tree, x, w, dy, with_bias=False, workspace=None, status=None, stream=None):
+    """Backward: returns (dx bf16 [N, C], dw fp32 [K, C], dbias fp32 [C] or None)."""
+    parent, node_len = tree
+    N, C = x.shape
+    K = w.shape[0]
+    _need(x, (plan.n_tokens, C), torch.bfloat16, "x")
+    _need(dy, (plan.n_tokens, C), torch.bfloat16, "dy")
+    _need(w, (K, C), torch.float32, "w")
+    if workspace is None:
+        workspace = torch.empty(tree_conv1d_bwd_workspace(plan, C), dtype=torch.uint8, device=x.device)
+    dx = torch.empty_like(x)
+    dw = torch.empty_like(w)
+    db = torch.empty(C, dtype=torch.float32, device=x.device) if with_bias else None
+    _check(_lib().tree_conv1d_bwd(plan.ref(), _ptr(parent), _ptr(node_len), _ptr(x), _ptr(w), _ptr(dy), C, K,
+                                  _ptr(workspace), _ptr(dx), _ptr(dw), _ptr(db), _ptr(status), _stream(stream)),
+           "tree_conv1d_bwd")
+    return dx, dw, db
+
+
+def tree_route_states(tree, final_states, stream=None):
+    """init[v] = final[nearest ancestor of v holding tokens] (zeros for roots); fp32 [n_nodes, S]."""
+    parent, node_len = tree
+    n, S = final_states.shape
+    _need(final_states, (parent.shape[0], S), torch.float32, "final_states")
+    init = torch.empty_like(final_states)
+    _check(_lib().tree_route_states(_ptr(parent), _ptr(node_len), n, _ptr(final_states), S, _ptr(init),
+                                    _stream(stream)), "tree_route_states")
+    return init
+
+
+def tree_route_states_bwd(tree, d_init, d_final=None, stream=None):
+    """d_final[ancestor(v)] += d_init[v]; returns d_final (zeros first when not given)."""
+    parent, node_len = tree
+    n, S = d_init.shape
+    _need(d_init, (parent.shape[0], S), torch.float32, "d_init")
+    d_final = torch.zeros_like(d_init) if d_final is None else d_final
+    _check(_lib().tree_route_states_bwd(_ptr(parent), _ptr(node_len), n, _ptr(d_init), S, _ptr(d_final),
+                                        _stream(stream)), "tree_route_states_bwd")
+    return d_final

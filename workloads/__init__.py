@@ -7,7 +7,7 @@ what is generated here as plain inputs.
 """
 from .trees import (CONFIGS, Workload, tiny_tree, caterpillar_tree, rollout_tree,
                     forest_tree, large_tree, random_tree, make_workload)
-from .tensors import make_tensors
+from .tensors import make_conv_tensors, make_tensors
 
 __all__ = ["CONFIGS", "Workload", "tiny_tree", "caterpillar_tree", "rollout_tree",
-           "forest_tree", "large_tree", "random_tree", "make_workload", "make_tensors"]
+           "forest_tree", "large_tree", "random_tree", "make_workload", "make_tensors", "make_conv_tensors"]

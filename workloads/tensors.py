@@ -31,3 +31,14 @@ def make_tensors(wl, n_tokens: int | None = None, with_fp32: bool = False):
     if with_fp32:
         out.update(q32=q32, k32=k32, v32=v32)
     return out
+
+
+def make_conv_tensors(n_tokens: int, C: int, K: int, seed: int = 0, with_bias: bool = True):
+    """Seeded inputs of a depthwise causal convolution over the packed tokens: x [N, C] and the
+    upstream gradient u [N, C] i.i.d. N(0, 1) rounded to bf16; taps w [K, C] N(0, 1/K) and
+    bias [C] N(0, 1) in fp32 (or None)."""
+    x = _randn(seed, (n_tokens, C)).to(torch.bfloat16)
+    u = _randn(seed + 1, (n_tokens, C)).to(torch.bfloat16)
+    w = _randn(seed + 2, (K, C)) / K ** 0.5
+    b = _randn(seed + 3, (C,)) if with_bias else None
+    return dict(x=x, w=w, bias=b, u=u)
