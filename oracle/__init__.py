@@ -18,6 +18,9 @@ Modules
                and the associative (max, numerator, denominator) softmax merge.
 ``hybrid``     section 9: the path-expanded causal convolution (forward and backward)
                and the parent-routed recurrent state with its transpose.
+``ce``         sections 6.2, 6.3, 12: the path-averaged next-token cross-entropy with ignore
+               labels (loss, logsumexp, gradients of the hidden states and the vocabulary
+               matrix), whole and restricted to sampled rows.
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py`` against the
 pages' worked example, closed forms, brute force on tiny inputs, library routines in
@@ -28,8 +31,9 @@ from .tree import (TreeError, validate_tree, root_to_leaf_paths, plan, tile_clas
 from .attention import (rope, rope_transpose, attention_paths, attention_nodes,
                         merge_softmax_state, softmax_state)
 from .hybrid import conv_paths, route_states, route_states_bwd
+from .ce import ce_paths, ce_rows
 
 __all__ = ["TreeError", "validate_tree", "root_to_leaf_paths", "plan", "tile_classes",
            "tree_stats", "TILE", "rope", "rope_transpose", "attention_paths",
            "attention_nodes", "merge_softmax_state", "softmax_state", "conv_paths",
-           "route_states", "route_states_bwd"]
+           "route_states", "route_states_bwd", "ce_paths", "ce_rows"]
