@@ -470,6 +470,117 @@ def conv_cpu_baseline(wl, t, budget_s=15.0):
                        f"{el:.1f} s; NumPy default threads")
 
 
+CE_METRIC = "tree next-token CE fused with the vocabulary projection, fwd+bwd TFLOP/s on 1 GB300 (6 N V D)"
+
+
+def run_ce(args, dev):
+    """The path-averaged next-token cross-entropy fused with the vocabulary projection (Tree
+    Training explainer, sections 6.2, 6.3, 12) on the workload's tree: h [N, D] bf16, W [V, D]
+    bf16, labels with 10 % ignored.  Algorithmic work 6 N V D (logits, dh, dW); the chunked
+    recompute executes 8 N V D on the tensor cores."""
+    import tree_masked_attention_plan_gb300 as tam
+    torch.cuda.set_device(dev)
+    wl = make_workload(args.config)
+    D, V, chunk = args.ce_hidden, args.ce_vocab, args.ce_chunk
+    plan = tam.tree_plan(wl.parent, wl.node_len, device=dev)
+    N = plan.n_tokens
+    tree = tam.tree_arrays(wl.parent, wl.node_len, dev)
+    gen = torch.Generator().manual_seed(13)
+    h_host = torch.randn(N, D, generator=gen).to(torch.bfloat16)
+    lab_host = torch.randint(0, V, (N,), generator=gen, dtype=torch.int32)
+    lab_host[torch.rand(N, generator=gen) < 0.1] = -100
+    gdev = torch.Generator(device=dev).manual_seed(14)
+    W = (torch.randn(V, D, generator=gdev, device=dev) / D ** 0.5).to(torch.bfloat16)
+    h, labels = h_host.to(dev), lab_host.to(dev)
+    ws = torch.empty(tam.tree_ce_workspace(plan, D, V, chunk), dtype=torch.uint8, device=dev)
+    out = (torch.empty(1, device=dev), torch.empty(N, device=dev), torch.empty_like(h),
+           torch.empty(V, D, dtype=torch.float32, device=dev))
+    status = tam.new_status(dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def step():
+        tam.tree_ce_fwd_bwd(plan, tree, h, W, labels, chunk=chunk, workspace=ws, out=out, status=status)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    tam.check_status(status, "ce warmup")
+    ms = []
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        for _ in range(args.steps):
+            flush.fill_(1.0)
+            e0.record(stream)
+            step()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms.append(e0.elapsed_time(e1))
+    clocks = clk.summary()
+    tam.check_status(status, "ce steps")
+    hp, lp = h_host.pin_memory(), lab_host.pin_memory()
+    loss_host = torch.empty(1).pin_memory()
+    e2e = []
+    for i in range(args.warmup + args.steps):
+        flush.fill_(1.0)
+        e0.record(stream)
+        h.copy_(hp, non_blocking=True)
+        labels.copy_(lp, non_blocking=True)
+        step()
+        loss_host.copy_(out[0], non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            e2e.append(e0.elapsed_time(e1))
+    t = float(np.mean(ms))
+    algo = 6.0 * N * V * D
+    executed = 8.0 * N * V * D
+    peaks = load_peaks()
+    achieved = executed / (t * 1e-3) / 1e12
+    line = {
+        "metric": CE_METRIC, "value": round(algo / (t * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 operands, fp32 accumulate",
+        "data": "synthetic (seeded tree, N(0,1) bf16 hidden states, N(0,1/D) vocabulary matrix, 10 % ignored labels)",
+        "config": {"workload": f"{wl.name} CE D={D} V={V} chunk={chunk}", "N": N, "D": D, "V": V, "chunk": chunk,
+                   "step": "tree_ce_fwd_bwd (loss, lse, dh, dW)",
+                   "l2": "operands larger than L2, and flushed between steps"},
+        "roofline": {"kernel": "tree_ce_fwd_bwd (four GEMMs per chunk + small kernels)", "bound": "tensor",
+                     "achieved": round(achieved, 1), "peak": peaks["bf16"], "unit": "TFLOP/s",
+                     "frac": round(achieved / peaks["bf16"], 4), "peak_source": f"{peaks['source']} bf16 burst",
+                     "traffic": None, "algorithmic": "8 N V D executed MMA flops per call (6 N V D + recompute)"},
+        "e2e": {"value": round(algo / (float(np.mean(e2e)) * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(float(np.mean(e2e)), 4), "h2d_bytes_per_step": N * D * 2 + N * 4,
+                "d2h_bytes_per_step": 4},
+        "gpu_launches": (4 + 6 * ((N + chunk - 1) // chunk) + 2) * args.steps, "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = ce_cpu_baseline(wl, h_host, W.cpu(), lab_host, budget_s=15.0)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def ce_cpu_baseline(wl, h, W, labels, budget_s=15.0):
+    """The oracle's row form (fp64 logits, logsumexp and dh rows) on as many rows as fit the
+    budget; credited 4 V D flops per row (its logits and dh products)."""
+    import oracle
+    p = oracle.plan(wl.parent, wl.node_len)
+    Wd = W.double().numpy()
+    hd = h.double().numpy()
+    lab = labels.numpy()
+    t0, done = time.perf_counter(), 0
+    while time.perf_counter() - t0 < budget_s and done < hd.shape[0]:
+        oracle.ce_rows(wl.parent, wl.node_len, hd, Wd, lab, range(done, done + 8), p=p)
+        done += 8
+    el = time.perf_counter() - t0
+    V, D = Wd.shape
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return dict(value=round(4.0 * V * D * done / el / 1e12, 6), unit="TFLOP/s", cores=cores, kind="oracle",
+                sample=f"{wl.name}: fp64 logits, logsumexp and dh for rows 0-{done - 1} of {hd.shape[0]}, {el:.1f} s "
+                       f"(after converting W to fp64); NumPy/BLAS default threads")
+
+
 def cpu_baseline_sample(config, budget_s=20.0):
     """The oracle as it stands, on the host cores: path-expanded fp64 attention fwd+bwd for q head 0
     over a prefix of the root-to-leaf paths that fits the time budget.  Credit: 14 d times the
@@ -508,6 +619,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--conv", action="store_true",
                     help="time the hybrid-layer tree convolution (forward + backward) instead of attention")
+    ap.add_argument("--ce", action="store_true",
+                    help="time the fused vocabulary-projection cross-entropy instead of attention")
+    ap.add_argument("--ce-hidden", type=int, default=4096)
+    ap.add_argument("--ce-vocab", type=int, default=128256)
+    ap.add_argument("--ce-chunk", type=int, default=8192)
     ap.add_argument("--conv-channels", type=int, default=8192)
     ap.add_argument("--conv-k", type=int, default=4)
     ap.add_argument("--partition", action="store_true",
@@ -526,6 +642,10 @@ def main():
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local)
+    if args.ce:
+        if world > 1:
+            raise SystemExit("--ce runs on one GPU")
+        return run_ce(args, dev)
     if args.conv:
         if world > 1:
             raise SystemExit("--conv runs on one GPU")

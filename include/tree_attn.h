@@ -307,8 +307,43 @@ int tree_route_states_bwd(const int32_t* parent, const int32_t* node_len, int32_
                           const float* d_init, int S, float* d_final, tree_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
+ * Loss: the tree's next-token cross-entropy fused with the vocabulary projection
+ * ("Tree Training 技术详解", sections 6.2, 6.3 and 12).  Each root-to-leaf path is a sequence
+ * whose tokens' logits predict the next token's label; the tree loss is the average of the
+ * paths' summed losses.  Equivalently, token u (label not ignore_index) is predicted by the
+ * logits row z_t = W h_t of t = prev(u), the token before u on its root path (u-1 inside a
+ * node; the parent's last token - nearest ancestor holding tokens - for a node's first token),
+ * with weight g_u / K (the plan's w); a root's first token is predicted by nothing.
+ * -------------------------------------------------------------------------------------*/
+
+/* Workspace bytes for tree_ce_fwd_bwd: per-token pairs, label logits, weight sums and LSE,
+ * plus one chunk's (max, sum exp) partials and bf16 logits gradients (chunk x V x 2 bytes). */
+size_t tree_ce_workspace(const tree_plan_t* plan, int D, int V, int chunk);
+
+/* Loss and gradients in one call, processed in chunks of `chunk` logits rows (a multiple of
+ * 128; the last chunk may be shorter).  Per chunk the logits GEMM runs twice (for the row
+ * logsumexp, then for the gradient), so no logits are stored; then dh rows = dz W and
+ * dW (+)= dz^T h.  Inputs: h [N][D] bf16 hidden states in packed order, W [V][D] bf16,
+ * labels [N] int32 (ignore_index or 0 <= y < V; any other value sets TREE_ERR_ARG in
+ * status_dev and is ignored).  Outputs: *loss (device fp32 scalar), lse [N] fp32 per-row
+ * logsumexp (may be NULL), dh [N][D] bf16, dW [V][D] fp32 (overwritten).  D a multiple of
+ * 256, V a multiple of 8 (else TREE_ERR_SHAPE); pointers 16-byte aligned (else
+ * TREE_ERR_ARG).  Rounding: logits and all sums in fp32, the logits gradient stored in bf16,
+ * the loss summed in fp64. */
+int tree_ce_fwd_bwd(const tree_plan_t* plan, const int32_t* parent, const int32_t* node_len,
+                    const tree_bf16* h, const tree_bf16* W, const int32_t* labels, int D, int V,
+                    int chunk, int ignore_index, void* workspace, float* loss, float* lse,
+                    tree_bf16* dh, float* dW, int32_t* status_dev, tree_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
  * Diagnostics
  * -------------------------------------------------------------------------------------*/
+
+/* The GEMM kernel behind tree_ce_fwd_bwd on its own: C [M][N] fp32 = op(A) op(B)^T with
+ * a_mn = 0: A stored [M][K], 1: A stored [K][M]; b_mn = 0: B stored [N][K], 1: B stored
+ * [K][N] (bf16, row-major).  M, N, K multiples of 8; pointers 16-byte aligned. */
+int tree_diag_gemm(const tree_bf16* A, const tree_bf16* B, int M, int N, int K, int a_mn, int b_mn,
+                   float* C, int32_t* status_dev, tree_stream_t stream);
 
 /* Device waits give up after this many nanoseconds and report TREE_ERR_TIMEOUT
  * (default 2e9).  Values < 1e5 are raised to 1e5.  Process-wide. */

@@ -8,11 +8,12 @@ functions carry the C entry points' names (``include/tree_attn.h``):
   tree_plan_query, tree_plan (pos_offset -> tree_plan_offset), tree_rope_fwd,
   tree_apply_weights, tree_attn_fwd, tree_attn_bwd_workspace, tree_attn_bwd,
   tree_attn_fwd_gateway, tree_attn_bwd_gateway, tree_relay_add, tree_gather_rows, tree_conv1d_fwd,
-  tree_conv1d_bwd_workspace, tree_conv1d_bwd, tree_route_states, tree_route_states_bwd, tree_selftest_timeout,
-  tree_set_wait_limit_ns
+  tree_conv1d_bwd_workspace, tree_conv1d_bwd, tree_route_states, tree_route_states_bwd, tree_ce_workspace,
+  tree_ce_fwd_bwd, tree_selftest_timeout, tree_set_wait_limit_ns (and diag_gemm -> tree_diag_gemm)
 
 Semantics follow "Tree Training 技术详解" (tingdeliu.github.io): DFS packing (section 3.2),
-tree mask (4.2), block table (4.3), depth positions (5), path-count weights (6.2).
+tree mask (4.2), block table (4.3), depth positions (5), path-count weights (6.2), the
+path-averaged next-token loss (6.2, 6.3, 12), hybrid layers (9).
 """
 from __future__ import annotations
 
@@ -103,6 +104,10 @@ def _lib():
         "tree_conv1d_bwd": (_i32, [P(PlanT), _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp]),
         "tree_route_states": (_i32, [_vp, _vp, _i32, _vp, _i32, _vp, _vp]),
         "tree_route_states_bwd": (_i32, [_vp, _vp, _i32, _vp, _i32, _vp, _vp]),
+        "tree_ce_workspace": (ctypes.c_size_t, [P(PlanT), _i32, _i32, _i32]),
+        "tree_ce_fwd_bwd": (_i32, [P(PlanT), _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp,
+                                   _vp, _vp, _vp]),
+        "tree_diag_gemm": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp]),
         "tree_set_wait_limit_ns": (_i32, [_i64]),
         "tree_set_timing_events": (_i32, [ctypes.POINTER(_vp), _i32]),
         "tree_selftest_timeout": (_i32, [_vp, _i64, _vp]),
@@ -461,3 +466,40 @@ def tree_route_states_bwd(tree, d_init, d_final=None, stream=None):
     _check(_lib().tree_route_states_bwd(_ptr(parent), _ptr(node_len), n, _ptr(d_init), S, _ptr(d_final),
                                         _stream(stream)), "tree_route_states_bwd")
     return d_final
+
+
+def tree_ce_workspace(plan: TreePlan, D, V, chunk):
+    """Bytes of workspace tree_ce_fwd_bwd needs."""
+    return int(_lib().tree_ce_workspace(plan.ref(), D, V, chunk))
+
+
+def tree_ce_fwd_bwd(plan: TreePlan, tree, h, W, labels, chunk=8192, ignore_index=-100, workspace=None, out=None,
+                    status=None, stream=None):
+    """Path-averaged next-token cross-entropy fused with the vocabulary projection.
+    h [N, D] bf16, W [V, D] bf16, labels [N] int32.  Returns (loss [1] fp32, lse [N] fp32,
+    dh [N, D] bf16, dW [V, D] fp32); `out` may supply those four tensors."""
+    parent, node_len = tree
+    N, D = h.shape
+    V = W.shape[0]
+    _need(h, (plan.n_tokens, D), torch.bfloat16, "h")
+    _need(W, (V, D), torch.bfloat16, "W")
+    _need(labels, (plan.n_tokens,), torch.int32, "labels")
+    if workspace is None:
+        workspace = torch.empty(tree_ce_workspace(plan, D, V, chunk), dtype=torch.uint8, device=h.device)
+    if out is None:
+        out = (torch.empty(1, dtype=torch.float32, device=h.device),
+               torch.empty(N, dtype=torch.float32, device=h.device), torch.empty_like(h),
+               torch.empty(V, D, dtype=torch.float32, device=h.device))
+    loss, lse, dh, dW = out
+    _check(_lib().tree_ce_fwd_bwd(plan.ref(), _ptr(parent), _ptr(node_len), _ptr(h), _ptr(W), _ptr(labels), D, V,
+                                  chunk, ignore_index, _ptr(workspace), _ptr(loss), _ptr(lse), _ptr(dh), _ptr(dW),
+                                  _ptr(status), _stream(stream)), "tree_ce_fwd_bwd")
+    return loss, lse, dh, dW
+
+
+def diag_gemm(A, B, M, N, K, a_mn, b_mn, status=None, stream=None):
+    """C [M, N] fp32 = op(A) op(B)^T on the library's GEMM kernel (a_mn: A is [K, M]; b_mn: B is [K, N])."""
+    C = torch.empty(M, N, dtype=torch.float32, device=A.device)
+    _check(_lib().tree_diag_gemm(_ptr(A), _ptr(B), M, N, K, int(a_mn), int(b_mn), _ptr(C), _ptr(status),
+                                 _stream(stream)), "tree_diag_gemm")
+    return C

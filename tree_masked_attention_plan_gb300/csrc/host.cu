@@ -120,6 +120,30 @@ int make_tmap_bf16_2d(CUtensorMap* m, const void* base, int inner, int rows, int
   return TREE_OK;
 }
 
+// 2-D map over a bf16 matrix [rows][inner] with the 128-byte swizzle (box_inner x 2 B <= 128),
+// the layout tcgen05 shared-memory descriptors read; out-of-range elements read as zero.
+int make_tmap_bf16_2d_sw128(CUtensorMap* m, const void* base, int inner, int rows, int box_inner, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) {
+    std::snprintf(g_last_err, sizeof(g_last_err), "cuTensorMapEncodeTiled entry point unavailable");
+    return TREE_ERR_CUDA;
+  }
+  if ((reinterpret_cast<uintptr_t>(base) & 15) != 0 || (inner * 2) % 16 != 0) return TREE_ERR_ARG;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    std::snprintf(g_last_err, sizeof(g_last_err), "cuTensorMapEncodeTiled (bf16 2-D sw128) failed (CUresult %d)",
+                  (int)r);
+    return TREE_ERR_CUDA;
+  }
+  return TREE_OK;
+}
+
 static cudaEvent_t g_events[4];
 static int g_n_events = 0;
 

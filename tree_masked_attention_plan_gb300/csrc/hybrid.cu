@@ -106,19 +106,25 @@ DEVI void drain_bar(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
 
 // Tile bookkeeping shared by both kernels.  A block owns one 256-channel slab (blockIdx.y) and
 // walks token tiles blockIdx.x, blockIdx.x + gridDim.x, ...  Two stages: while tile i is
-// computed, tile i+1's rows are in flight (one 2-D TMA load per staged tensor) and its
-// per-token node offsets are read into shared memory.
-//   meta[t] = (t - first token of t's node, tokens from t to the node's end)
-DEVI void tile_meta(const ConvArgs& a, int T0, int TB, int2* meta) {
-  for (int i = threadIdx.x; i < TB; i += blockDim.x) {
-    const int t = T0 + i;
-    int2 m = make_int2(0, 0);
-    if (t < a.N) {
-      const int v = a.tok_node[t];
-      const int s = a.tok_start[v];
-      m = make_int2(t - s, s + a.node_len[v] - t);
-    }
-    meta[i] = m;
+// computed, tile i+1's rows are in flight (one 2-D TMA load per staged tensor) and so are its
+// node ids (4-byte cp.async copies, one commit group per tile).  A node's tokens are
+// contiguous in packed order, so "t-k is in t's node" is ids[t-k] == ids[t]: no lookups of the
+// node's extent on the fast path.
+//   ids[m] = node of token T0 - (K-1) + m, or -1 outside [0, N)
+DEVI void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+DEVI void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+DEVI void cp_async_wait_prev() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }   // all but the newest
+DEVI void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+DEVI void stage_ids(const ConvArgs& a, int first, int count, int* ids) {
+  for (int m = threadIdx.x; m < count; m += blockDim.x) {
+    const int t = first + m;
+    if (t >= 0 && t < a.N)
+      cp_async4(ids + m, a.tok_node + t);
+    else
+      ids[m] = -1;
   }
 }
 
@@ -135,8 +141,9 @@ __global__ void __launch_bounds__(256) k_conv_fwd(const __grid_constant__ CUtens
   const int STAGE = round_stage(BOX);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_smem(smem_raw);
+  constexpr int NIDS = TB + K - 1;               // ids of rows [T0-(K-1), T0+TB)
   __shared__ uint64_t bars[2];
-  __shared__ int2 meta[2][TB];
+  __shared__ int ids[2][NIDS];
   __shared__ int abort_flag;
   const int CV = a.C / 8;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -167,7 +174,8 @@ __global__ void __launch_bounds__(256) k_conv_fwd(const __grid_constant__ CUtens
     mbar_expect_tx(&bars[0], BOX);
     tma_load_2d(smem, &tmX, &bars[0], blockIdx.y * 256, tile * TB - (K - 1));
   }
-  if (tile < n_tiles) tile_meta(a, tile * TB, TB, meta[0]);
+  if (tile < n_tiles) stage_ids(a, tile * TB - (K - 1), NIDS, ids[0]);
+  cp_async_commit();
   int i = 0;
   bool aborted = false;
   for (; tile < n_tiles; ++i, tile += gridDim.x) {
@@ -178,8 +186,10 @@ __global__ void __launch_bounds__(256) k_conv_fwd(const __grid_constant__ CUtens
         mbar_expect_tx(&bars[s ^ 1], BOX);
         tma_load_2d(smem + (s ^ 1) * STAGE, &tmX, &bars[s ^ 1], blockIdx.y * 256, next * TB - (K - 1));
       }
-      tile_meta(a, next * TB, TB, meta[s ^ 1]);
+      stage_ids(a, next * TB - (K - 1), NIDS, ids[s ^ 1]);
     }
+    cp_async_commit();
+    cp_async_wait_prev();
     const bool ok = mbar_wait(&bars[s], (i >> 1) & 1, wc);
     if (__syncthreads_or(!ok)) {
       aborted = true;
@@ -192,11 +202,10 @@ __global__ void __launch_bounds__(256) k_conv_fwd(const __grid_constant__ CUtens
       for (int r = warp; r < TB; r += kConvWarps) {
         const int t = T0 + r;
         if (t >= a.N) break;
-        const int off = meta[s][r].x;
         float acc[8], xv[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = b[e];
-        if (off >= K - 1) {
+        if (ids[s][r] == ids[s][r + K - 1]) {     // t-K+1 .. t all in t's node
 #pragma unroll
           for (int k = 0; k < K; ++k) {
             load8(reinterpret_cast<const uint4*>(xs + (r + K - 1 - k) * rs), xv);
@@ -217,6 +226,7 @@ __global__ void __launch_bounds__(256) k_conv_fwd(const __grid_constant__ CUtens
     }
     __syncthreads();
   }
+  cp_async_wait_all();
   if (aborted && threadIdx.x == 0) {
     drain_bar(&bars[i & 1], (i >> 1) & 1, limit_ns);
     if (tile + gridDim.x < n_tiles) drain_bar(&bars[(i & 1) ^ 1], ((i + 1) >> 1) & 1, limit_ns);
@@ -243,8 +253,9 @@ __global__ void __launch_bounds__(256) k_conv_bwd(const __grid_constant__ CUtens
   const int HALF = round_stage(BOX), STAGE = 2 * HALF;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_smem(smem_raw);
+  constexpr int NIDS = TB + 2 * (K - 1);         // ids of rows [T0-(K-1), T0+TB+K-1)
   __shared__ uint64_t bars[2];
-  __shared__ int2 meta[2][TB];
+  __shared__ int ids[2][NIDS];
   __shared__ int abort_flag;
   __shared__ __align__(16) float red[kConvWarps][32 * 8];
   const int CV = a.C / 8;
@@ -281,7 +292,8 @@ __global__ void __launch_bounds__(256) k_conv_bwd(const __grid_constant__ CUtens
   };
   int tile = blockIdx.x;
   if (threadIdx.x == 0 && tile < n_tiles) issue(tile, 0);
-  if (tile < n_tiles) tile_meta(a, tile * TB, TB, meta[0]);
+  if (tile < n_tiles) stage_ids(a, tile * TB - (K - 1), NIDS, ids[0]);
+  cp_async_commit();
   int i = 0;
   bool aborted = false;
   for (; tile < n_tiles; ++i, tile += gridDim.x) {
@@ -289,8 +301,10 @@ __global__ void __launch_bounds__(256) k_conv_bwd(const __grid_constant__ CUtens
     const int next = tile + gridDim.x;
     if (next < n_tiles) {
       if (threadIdx.x == 0) issue(next, s ^ 1);
-      tile_meta(a, next * TB, TB, meta[s ^ 1]);
+      stage_ids(a, next * TB - (K - 1), NIDS, ids[s ^ 1]);
     }
+    cp_async_commit();
+    cp_async_wait_prev();
     const bool ok = mbar_wait(&bars[s], (i >> 1) & 1, wc);
     if (__syncthreads_or(!ok)) {
       aborted = true;
@@ -304,19 +318,22 @@ __global__ void __launch_bounds__(256) k_conv_bwd(const __grid_constant__ CUtens
       for (int r = warp; r < TB; r += kConvWarps) {
         const int t = T0 + r;
         if (t >= a.N) break;
-        const int off = meta[s][r].x, rem = meta[s][r].y;
+        const int* id = ids[s] + r;               // id[K-1] is t's node; id[K-1-k] token t-k, id[K-1+k] t+k
+        const int v = id[K - 1];
         float g[8], xv[8], acc[8];
         load8(reinterpret_cast<const uint4*>(ds + r * rs), g);
 #pragma unroll
         for (int e = 0; e < 8; ++e) dbl[e] += g[e];
         // dw (and, for the first K-1 tokens of a node, the terms that cross into an ancestor)
-        if (off >= K - 1) {
+        if (id[0] == v) {
 #pragma unroll
           for (int k = 0; k < K; ++k) {
             load8(reinterpret_cast<const uint4*>(xs + (r + K - 1 - k) * rs), xv);
             fma8(dwl[k], xv, g);
           }
         } else {
+          int off = 0;                            // tokens of v before t (< K-1 here)
+          while (off < K - 1 && id[K - 2 - off] == v) ++off;
           int j = t;
 #pragma unroll
           for (int k = 0; k < K; ++k) {
@@ -335,7 +352,7 @@ __global__ void __launch_bounds__(256) k_conv_bwd(const __grid_constant__ CUtens
         // dx: the successors inside the node, all staged (t + k < node end <= N)
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = wr[0][e] * g[e];
-        if (rem >= K) {
+        if (id[2 * (K - 1)] == v) {               // t .. t+K-1 all in t's node
 #pragma unroll
           for (int k = 1; k < K; ++k) {
             load8(reinterpret_cast<const uint4*>(ds + (r + k) * rs), xv);
@@ -345,7 +362,7 @@ __global__ void __launch_bounds__(256) k_conv_bwd(const __grid_constant__ CUtens
         } else {
 #pragma unroll
           for (int k = 1; k < K; ++k) {
-            if (k >= rem) break;
+            if (id[K - 1 + k] != v) break;          // t+k past the node's end
             load8(reinterpret_cast<const uint4*>(ds + (r + k) * rs), xv);
             fma8(acc, wr[k], xv);
           }
@@ -355,6 +372,7 @@ __global__ void __launch_bounds__(256) k_conv_bwd(const __grid_constant__ CUtens
     }
     __syncthreads();
   }
+  cp_async_wait_all();
   if (aborted) {
     if (threadIdx.x == 0) {
       drain_bar(&bars[i & 1], (i >> 1) & 1, limit_ns);
@@ -389,22 +407,21 @@ __global__ void __launch_bounds__(256) k_conv_bwd(const __grid_constant__ CUtens
 }
 
 // The boundary rows of node v: its last min(len, K-1) tokens.  Zeroed before k_conv_bwd (and dw,
-// dbias by block 0), converted to bf16 after it.  Block per node (grid-stride), threads over the
-// rows' channels.
+// dbias by block (0, 0)), converted to bf16 after it.  Blocks over nodes (x, grid-stride) and
+// chunks of the rows' channels (y).
 __global__ void __launch_bounds__(256) k_conv_bwd_zero(ConvArgs a, float* ws, float* dw, float* dbias) {
   const int C4 = a.C / 4;
+  const int i0 = blockIdx.y * blockDim.x + threadIdx.x, step = gridDim.y * blockDim.x;
   if (blockIdx.x == 0) {
-    for (int i = threadIdx.x; i < a.K * C4; i += blockDim.x)
-      reinterpret_cast<float4*>(dw)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = i0; i < a.K * C4; i += step) reinterpret_cast<float4*>(dw)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (dbias)
-      for (int i = threadIdx.x; i < C4; i += blockDim.x)
-        reinterpret_cast<float4*>(dbias)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int i = i0; i < C4; i += step) reinterpret_cast<float4*>(dbias)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   for (int v = blockIdx.x; v < a.n_nodes; v += gridDim.x) {
     const int len = a.node_len[v];
     const int rows = min(len, a.K - 1);
     const size_t r0 = (size_t)(a.tok_start[v] + len - rows);
-    for (int i = threadIdx.x; i < rows * C4; i += blockDim.x)
+    for (int i = i0; i < rows * C4; i += step)
       reinterpret_cast<float4*>(ws + r0 * a.C)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
@@ -412,11 +429,12 @@ __global__ void __launch_bounds__(256) k_conv_bwd_zero(ConvArgs a, float* ws, fl
 __global__ void __launch_bounds__(256) k_conv_bwd_finish(ConvArgs a, const float* __restrict__ ws,
                                                          uint2* __restrict__ dx) {
   const int C4 = a.C / 4;
+  const int i0 = blockIdx.y * blockDim.x + threadIdx.x, step = gridDim.y * blockDim.x;
   for (int v = blockIdx.x; v < a.n_nodes; v += gridDim.x) {
     const int len = a.node_len[v];
     const int rows = min(len, a.K - 1);
     const size_t r0 = (size_t)(a.tok_start[v] + len - rows);
-    for (int i = threadIdx.x; i < rows * C4; i += blockDim.x) {
+    for (int i = i0; i < rows * C4; i += step) {
       const float4 f = reinterpret_cast<const float4*>(ws + r0 * a.C)[i];
       dx[r0 * C4 + i] = make_uint2(pack_bf16(f.x, f.y), pack_bf16(f.z, f.w));
     }
@@ -554,7 +572,8 @@ int tree_conv1d_bwd(const tree_plan_t* plan, const int32_t* parent, const int32_
   if (rc) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   float* ws = static_cast<float*>(workspace);
-  const unsigned node_blocks = (unsigned)std::max(1, std::min(a.n_nodes, 152 * 8));
+  const int row_chunks = std::max(1, std::min(16, ((std::max(K - 1, 1)) * (C / 4) + 255) / 256));
+  const dim3 node_blocks((unsigned)std::max(1, std::min(a.n_nodes, 152 * 8)), (unsigned)row_chunks);
   k_conv_bwd_zero<<<node_blocks, 256, 0, s>>>(a, ws, dw, dbias);
   rc = record_cuda(cudaGetLastError());
   if (rc) return rc;
