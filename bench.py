@@ -11,6 +11,10 @@ per visible query-key pair per q head; N_pairs = sum_t (pos_t + 1)), plus tokens
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
 Under torchrun each rank runs its own tree (weak scaling, no data-path collective); rank 0
 prints one JSON line with the max-over-ranks time.
+
+Other single-GPU lines on the same tree: --partition (the tree as gateway partitions), --conv
+(hybrid-layer causal convolution forward + backward, algorithmic GB/s), --ce (next-token
+cross-entropy fused with the vocabulary projection, TFLOP/s).
 """
 from __future__ import annotations
 

@@ -1,6 +1,7 @@
 // Path-averaged next-token cross-entropy over the packed tree ("Tree Training 技术详解",
 // sections 6.2, 6.3, 12), fused with the vocabulary projection and computed chunk by chunk
-// so that only one chunk of logits gradients is ever materialised.
+// so that only one chunk of logits gradients is ever materialised (the chunked, recomputed
+// logits of the agent-RL tutorial, chapter 14 "规模扩展与效率", section 14.3).
 //
 // Pairs: token u (label not ignored) is predicted by the logits row of prev(u), the token
 // before u on its root path (u-1 inside a node, the parent's last token for a node's first
