@@ -140,3 +140,47 @@ def test_hybrid_entry_points_reject_bad_arguments_without_a_gpu(lib):
     assert g(a, a, 0, a, 8, a, None) == -6
     assert lib.tree_conv1d_fwd(None, None, None, None, None, None, 8, 4, None, None, None) != 0
     assert lib.tree_conv1d_bwd_workspace(None, 8) == 0
+
+
+def _fake_plan(n_tokens=300, n_paths=2, n_nodes=4):
+    """A plan descriptor whose pointers are never dereferenced by the host-side checks."""
+    c = tam.PlanT()
+    for f in tam.PLAN_PTR_FIELDS:
+        setattr(c, f, 4096 * 16)
+    c.n_nodes, c.n_tokens, c.n_tiles, c.n_paths = n_nodes, n_tokens, (n_tokens + 127) // 128, n_paths
+    return c
+
+
+def test_loss_and_conv_entry_points_check_shapes_before_any_cuda_call(lib):
+    L = tam._lib()
+    plan = ctypes.byref(_fake_plan())
+    a = 4096 * 64                                     # 16-byte aligned stand-in address
+    ce = lambda D, V, chunk, h=a, W=a: L.tree_ce_fwd_bwd(plan, a, a, h, W, a, D, V, chunk, -100, a, a, a, a, a, None,
+                                                         None)
+    assert ce(200, 1000, 256) == -2                   # D not a multiple of 256
+    assert ce(256, 1001, 256) == -2                   # V not a multiple of 8
+    assert ce(256, 1000, 100) == -2                   # chunk not a multiple of 128
+    assert ce(256, 1000, 256, h=a + 8) == -6          # misaligned
+    assert ce(256, 1000, 256, W=None) == -6           # NULL
+    conv = lambda C, K, par=a: L.tree_conv1d_fwd(plan, par, a, a, a, None, C, K, a, None, None)
+    assert conv(12, 4) == -2 and conv(16, 9) == -2 and conv(16, 0) == -2
+    assert conv(16, 4, par=None) == -6
+    bwd = L.tree_conv1d_bwd(plan, a, a, a, a, a, 16, 4, None, a, a, None, None, None)
+    assert bwd == -6                                  # no workspace
+    assert L.tree_diag_gemm(a, a, 7, 8, 8, 0, 0, a, None, None) == -2
+    assert L.tree_diag_gemm(None, a, 8, 8, 8, 0, 0, a, None, None) == -6
+    assert L.tree_conv1d_fwd(None, a, a, a, a, None, 16, 4, a, None, None) == -6   # no plan
+
+
+def test_loss_workspace_size_is_host_arithmetic(lib):
+    L = tam._lib()
+    N = 300
+    plan = ctypes.byref(_fake_plan(N))
+    small = L.tree_ce_workspace(plan, 256, 1000, 128)
+    whole = L.tree_ce_workspace(plan, 256, 1000, 1 << 20)
+    assert 0 < small < whole
+    assert whole == L.tree_ce_workspace(plan, 256, 1000, N)          # chunks longer than the tree clamp to N
+    # the per-chunk logits gradient dominates: growing the chunk by 128 rows adds 128 x V bf16
+    assert L.tree_ce_workspace(plan, 256, 1000, 256) - small >= 128 * 1000 * 2
+    assert L.tree_ce_workspace(None, 256, 1000, 128) == 0
+    assert L.tree_conv1d_bwd_workspace(plan, 64) == N * 64 * 4

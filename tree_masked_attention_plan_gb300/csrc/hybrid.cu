@@ -470,7 +470,7 @@ int conv_args(const tree_plan_t* plan, const int32_t* parent, const int32_t* nod
   if (!parent || !node_len) return TREE_ERR_ARG;
   if (C <= 0 || C % 8 != 0 || K < 1 || K > kConvMaxK) return TREE_ERR_SHAPE;
   *a = ConvArgs{plan->tok_node, plan->tok_start, parent, node_len, plan->n_tokens, C, K, plan->n_nodes};
-  return check_device();
+  return TREE_OK;
 }
 
 bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) != 0; }
@@ -535,6 +535,8 @@ int tree_conv1d_fwd(const tree_plan_t* plan, const int32_t* parent, const int32_
   if (rc) return rc;
   if (!x || !w || !y || misaligned(x) || misaligned(w) || misaligned(y) || (bias && misaligned(bias)))
     return TREE_ERR_ARG;
+  rc = check_device();
+  if (rc) return rc;
   CUtensorMap tx;
   rc = make_tmap_bf16_2d(&tx, x, C, a.N, conv_box(C), kConvFwdTile + K - 1);
   if (rc) return rc;
@@ -566,6 +568,8 @@ int tree_conv1d_bwd(const tree_plan_t* plan, const int32_t* parent, const int32_
                         (const void*)dw})
     if (misaligned(p)) return TREE_ERR_ARG;
   if (dbias && misaligned(dbias)) return TREE_ERR_ARG;
+  rc = check_device();
+  if (rc) return rc;
   CUtensorMap tx, tdy;
   rc = make_tmap_bf16_2d(&tx, x, C, a.N, conv_box(C), kConvBwdTile + K - 1);
   if (!rc) rc = make_tmap_bf16_2d(&tdy, dy, C, a.N, conv_box(C), kConvBwdTile + K - 1);
