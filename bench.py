@@ -557,7 +557,8 @@ def run_ce(args, dev):
         "e2e": {"value": round(algo / (float(np.mean(e2e)) * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(float(np.mean(e2e)), 4), "h2d_bytes_per_step": N * D * 2 + N * 4,
                 "d2h_bytes_per_step": 4},
-        "gpu_launches": (4 + 6 * ((N + chunk - 1) // chunk) + 2) * args.steps, "clocks": clocks,
+        # pairs, label logits, loss, loss out + per chunk: 4 GEMMs, LSE merge, label fix-up
+        "gpu_launches": (4 + 6 * ((N + chunk - 1) // chunk)) * args.steps, "clocks": clocks,
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = ce_cpu_baseline(wl, h_host, W.cpu(), lab_host, budget_s=15.0)

@@ -7,9 +7,10 @@ sections 6.2, 6.3, 12) with the oracle, and of the GEMM kernel under it.
   shorter than the tree (the last one ragged), one chunk, and all labels ignored: loss, row
   logsumexp, dh and dW against the fp64 oracle;
 * rollout32k at full size (N = 32768, D = 4096, V = 128256, chunks of 8192): the oracle's
-  logsumexp and dh on sampled rows; over all of dW, the identity sum_v dW[v] = 0 (each row of
-  the logits gradient sums to zero); the loss equals sum_u c_u (LSE - z_label) evaluated by the
-  oracle on the sampled rows' share.
+  logsumexp and dh on sampled rows (chunk edges and nodes' last tokens, which predict several
+  children); over all of dW, the identity sum_v dW[v] = 0 (each row of the logits gradient
+  sums to zero); the loss finite and positive (its value needs every row's logsumexp, which
+  the small-size cases check against the oracle).
 
 Tolerances: logits are fp32 sums of bf16 products (~1e-6 relative); the logits gradient is
 stored in bf16 (2^-9 relative per element), so dh and dW are compared at 2e-2 of their largest
