@@ -38,10 +38,9 @@ from workloads import CONFIGS, make_tensors, make_workload  # noqa: E402
 METRIC = "tree-attn fwd+bwd visible-pair TFLOP/s and tokens/s on 1 GB300; % of bf16 peak"
 UNIT = "TFLOP/s"
 DEFAULT_CONFIG = "rollout32k"
-# kernels of this library per step: plan (expand, zero, hi range, node runs, rows, cols, scan and
-# orders, fill), RoPE, forward, loss weights, backward (delta and dQ-accumulator zeroing, dK/dV,
-# dQ finalize)
-LAUNCHES_PER_STEP = 8 + 1 + 1 + 1 + 3
+# kernels of this library per step: plan (tokens with per-tile data, classes, lists and orders),
+# RoPE, forward, loss weights, backward (delta and dQ-accumulator zeroing, dK/dV, dQ finalize)
+LAUNCHES_PER_STEP = 3 + 1 + 1 + 1 + 3
 DKDV_PROFILE = os.path.join(ROOT, "profiles", "k_bwd_dkdv_rollout32k.md")
 DKDV_SOURCES = [os.path.join(ROOT, "tree_masked_attention_plan_gb300", "csrc", f) for f in ("attn_bwd.cu", "common.cuh")]
 

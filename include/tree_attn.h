@@ -67,7 +67,9 @@ typedef struct {
   int32_t n_tiles;    /* T = ceil(N / 128) */
   int32_t n_paths;    /* K = root-to-leaf paths (leaves of all roots) */
   int64_t max_nnz;    /* T (T + 1) / 2: capacity of row_idx / col_idx */
-  int64_t plan_bytes; /* device bytes tree_plan_bind() carves the plan arrays from */
+  int64_t plan_bytes; /* device bytes tree_plan_bind() carves the plan arrays from (the
+                         arrays below plus 12 T bytes of per-tile counts tree_plan uses
+                         as scratch, placed after `counts`) */
 } tree_plan_info;
 
 /* Host-side descriptor of a plan; every pointer is device memory inside the buffer given
@@ -116,6 +118,15 @@ typedef struct {
 int tree_plan_query(const int32_t* parent, const int32_t* node_len, int32_t n_nodes,
                     tree_plan_info* info);
 
+/* The plan's per-node arrays, computed on the host exactly as tree_plan computes them before
+ * copying them to the device (section 3.2: depth-first preorder with children by ascending id,
+ * roots by ascending id; section 4.3 intervals; section 5 depth offsets; section 6.2 leaf
+ * counts).  Host only, no CUDA call.  `out` is caller-owned host memory of 8 * n_nodes int32
+ * and receives, n_nodes each and in this order: order, dfs_in, dfs_out, tok_start, depth_off,
+ * leaves, dfs_tok_start, sub_end (the fields of tree_plan_t with the same names).  Invalid
+ * trees as tree_plan_query; out == NULL -> TREE_ERR_ARG. */
+int tree_plan_nodes(const int32_t* parent, const int32_t* node_len, int32_t n_nodes, int32_t* out);
+
 /* Carve the plan arrays out of a caller-owned device buffer of info->plan_bytes bytes
  * (256-byte aligned) and fill `plan`'s pointers and sizes.  Host only, no CUDA call. */
 int tree_plan_bind(const tree_plan_info* info, void* device_buffer, tree_plan_t* plan);
@@ -123,8 +134,9 @@ int tree_plan_bind(const tree_plan_info* info, void* device_buffer, tree_plan_t*
 /* Build the plan on `stream` (sections 3.2, 4.3, 5, 6.2 of the explainer):
  *   host:   validation, depth-first preorder (children by ascending id), dfs_in/dfs_out,
  *           tok_start, depth_off, leaves, sub_end; one async copy of these to the device;
- *   device: per-token expansion (tok_node, pos, g, w, tok_in, tok_out, hi), per-key-tile
- *           hi range, tile classes, row/column CSR lists and heaviest-first orders.
+ *   device: three launches: per-token expansion (tok_node, pos, g, w, tok_in, tok_out,
+ *           hi) with the per-key-tile hi range and node runs; tile classes with per-row and
+ *           per-column counts; row/column CSR lists and heaviest-first orders.
  * `plan` must come from tree_plan_bind() for the same tree.  The host arrays may be freed
  * when the call returns. */
 int tree_plan(const int32_t* parent, const int32_t* node_len, int32_t n_nodes,
@@ -247,8 +259,10 @@ int tree_gather_rows(const int32_t* rows, int32_t n, const tree_bf16* src, tree_
  *   - Size limit: a problem whose tree_attn_bwd_workspace() exceeds the array is rejected
  *     with TREE_ERR_SCRATCH before anything is launched (at d = 128, Hq = 32 that is about
  *     4000 tokens).
- *   - Set-up: the first call on each device looks up the array's device address (with that
- *     device current) and caches it; make that first call before any stream capture.
+ *   - Set-up: every call looks up the array's device address in the current device's
+ *     context (a host-side symbol lookup, no allocation), so the address stays right after
+ *     cudaDeviceReset.  The first call on a device may load the library's device code into
+ *     that context: make it before any stream capture.
  *   - Sharing: every call on a device uses the same array, which keeps the last call's
  *     contents (the accumulator is cleared at the start of each call).  Calls that overlap
  *     on the GPU (different streams, or different host threads without ordering) race on

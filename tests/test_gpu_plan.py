@@ -16,7 +16,9 @@ def _trees():
            ("ragged129", (np.array([-1, 0, 0]), np.array([1, 64, 64]))),
            ("chain", (np.array([-1] + list(range(299))), np.full(300, 3))),
            ("star", (np.array([-1] + [0] * 400), np.r_[50, np.arange(400) % 7])),
-           ("zero_root", (np.array([-1, 0, 0, 1]), np.array([0, 5, 0, 300])))]
+           ("zero_root", (np.array([-1, 0, 0, 1]), np.array([0, 5, 0, 300]))),
+           ("star_1100_tiles", (np.array([-1] + [0] * 1100), np.full(1101, 128))),
+           ("forest_1200_tiles", (np.full(600, -1), np.full(600, 256)))]
     for s in range(24):
         out.append((f"rand{s}", random_tree(1000 + s, n_nodes=2 + 7 * s, max_len=40 + 10 * s,
                                             zero_prob=0.1 if s % 3 == 0 else 0.0, n_roots=1 + (s % 5 == 2) * 3)))

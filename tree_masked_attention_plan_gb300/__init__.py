@@ -31,7 +31,7 @@ MAX_RUNS = 16
 
 TREE_OK = 0
 ERROR_NAMES = {-1: "TREE_ERR_INVALID_TREE", -2: "TREE_ERR_SHAPE", -3: "TREE_ERR_ARCH", -4: "TREE_ERR_CUDA",
-               -5: "TREE_ERR_TIMEOUT", -6: "TREE_ERR_ARG"}
+               -5: "TREE_ERR_TIMEOUT", -6: "TREE_ERR_ARG", -7: "TREE_ERR_SCRATCH"}
 
 _i32, _i64, _vp, _f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_float
 
@@ -85,6 +85,7 @@ def _lib():
     sig = {
         "tree_plan_query": (_i32, [_vp, _vp, _i32, P(PlanInfo)]),
         "tree_plan_bind": (_i32, [P(PlanInfo), _vp, P(PlanT)]),
+        "tree_plan_nodes": (_i32, [_vp, _vp, _i32, _vp]),
         "tree_plan": (_i32, [_vp, _vp, _i32, P(PlanT), _vp]),
         "tree_plan_offset": (_i32, [_vp, _vp, _i32, _i32, P(PlanT), _vp]),
         "tree_rope_fwd": (_i32, [P(PlanT), _vp, _vp, _vp, _vp, _i32, _i32, _i32, _f32, _vp]),
@@ -150,6 +151,20 @@ def tree_plan_query(parent, node_len) -> dict:
     _check(_lib().tree_plan_query(par.ctypes.data, nl.ctypes.data, len(par), ctypes.byref(info)),
            "tree_plan_query")
     return {f: getattr(info, f) for f, _ in PlanInfo._fields_}
+
+
+NODE_FIELDS = ["order", "dfs_in", "dfs_out", "tok_start", "depth_off", "leaves", "dfs_tok_start", "sub_end"]
+
+
+def tree_plan_nodes(parent, node_len) -> dict:
+    """The plan's per-node arrays (depth-first order, intervals, token starts, depth offsets,
+    leaf counts, subtree ends) from the library's host pass, as int64 NumPy arrays by name."""
+    par, nl = _host_i32(parent), _host_i32(node_len)
+    if par.shape != nl.shape:
+        raise ValueError("parent and node_len differ in length")
+    out = np.empty(8 * len(par), dtype=np.int32)
+    _check(_lib().tree_plan_nodes(par.ctypes.data, nl.ctypes.data, len(par), out.ctypes.data), "tree_plan_nodes")
+    return {f: out[i * len(par):(i + 1) * len(par)].astype(np.int64) for i, f in enumerate(NODE_FIELDS)}
 
 
 @dataclass
@@ -323,7 +338,7 @@ def check_status(status, where="device"):
         raise TreeError(code, where)
 
 
-__all__ = ["TreeError", "TreePlan", "tree_plan_query", "tree_plan", "tree_rope_fwd", "tree_apply_weights",
+__all__ = ["TreeError", "TreePlan", "tree_plan_query", "tree_plan_nodes", "tree_plan", "tree_rope_fwd", "tree_apply_weights",
            "tree_attn_fwd", "tree_attn_bwd_workspace", "tree_attn_bwd", "tree_set_wait_limit_ns",
            "tree_selftest_timeout", "tree_set_timing_events", "new_status", "check_status", "LIB_PATH", "TILE"]
 

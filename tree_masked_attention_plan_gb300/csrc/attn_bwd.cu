@@ -13,7 +13,8 @@
 //                    dV  += P^T dO           (cols 256..256+d)     accumulated on chip,
 //                    dK  += dS^T Q           (cols 256+d..256+2d)  written once at the end,
 //                    dQ   = dS K             (cols 128..128+d, lane = query), added to the fp32
-//                                            accumulator with coalesced red.global.add.
+//                                            accumulator by TMA bulk reduce-adds of 8 KiB pieces
+//                                            staged through shared memory.
 //                  The steps are software-pipelined: the tensor core runs dQ, dK of step n-1,
 //                  dP, dV of step n and S of step n+1 around the elementwise passes (P, then dS).
 //                  dK gets the inverse RoPE rotation in the epilogue.
@@ -577,18 +578,29 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
         tmem_load16(tmem + lane_off + C::DK_COL + c0, a);
         tmem_load16(tmem + lane_off + C::DK_COL + HD / 2 + c0, b);
         if (live) {
+          float lo[16], hi[16];
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
             const float g1 = __uint_as_float(a[c]), g2 = __uint_as_float(b[c]);
-            float lo = g1, hi = g2;
+            lo[c] = g1;
+            hi[c] = g2;
             if (p.rope_theta > 0.f) {
               float sv, cv;
               sincosf(posf * rope_inv_freq(c0 + c, HD, p.rope_theta), &sv, &cv);
-              lo = g1 * cv + g2 * sv;
-              hi = g2 * cv - g1 * sv;
+              lo[c] = g1 * cv + g2 * sv;
+              hi[c] = g2 * cv - g1 * sv;
             }
-            dkg[c0 + c] += lo;
-            dkg[HD / 2 + c0 + c] += hi;
+          }
+          // 16 consecutive fp32 of each half row: four 16-byte read-add-writes per half
+          float4* d4 = reinterpret_cast<float4*>(dkg + c0);
+          float4* e4 = reinterpret_cast<float4*>(dkg + HD / 2 + c0);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            float4 t = d4[v], u = e4[v];
+            t.x += lo[4 * v]; t.y += lo[4 * v + 1]; t.z += lo[4 * v + 2]; t.w += lo[4 * v + 3];
+            u.x += hi[4 * v]; u.y += hi[4 * v + 1]; u.z += hi[4 * v + 2]; u.w += hi[4 * v + 3];
+            d4[v] = t;
+            e4[v] = u;
           }
         }
       }
@@ -871,28 +883,18 @@ extern "C" int tree_relay_add(const int32_t* rows, int32_t len, const float* dk_
 // from one fixed device array instead of a caller workspace (for callers that cannot
 // allocate device memory).  The array is shared by every call on a device; the accumulator
 // is zeroed at the start of each call, and overlapping calls race on it.
-#include <mutex>
-
 namespace ta {
 namespace {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[TREE_NOALLOC_SCRATCH_BYTES];
-std::mutex g_noalloc_mu;
-void* g_noalloc_addr[64];            // device address of the array, per device ordinal
 
-// Looks the array's address up once per device, with that device current.
+// The array's device address in the current device's context.  It is looked up on every call
+// (a host-side symbol lookup that allocates nothing) rather than cached: after cudaDeviceReset,
+// or any other teardown of the context, the module is loaded again and the array may move.
 int noalloc_scratch(void** out) {
-  int dev = 0;
-  int rc = record_cuda(cudaGetDevice(&dev));
+  void* p = nullptr;
+  const int rc = record_cuda(cudaGetSymbolAddress(&p, g_noalloc_scratch));
   if (rc) return rc;
-  if (dev < 0 || dev >= 64) return TREE_ERR_ARG;
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_addr[dev]) {
-    void* p = nullptr;
-    rc = record_cuda(cudaGetSymbolAddress(&p, g_noalloc_scratch));
-    if (rc) return rc;
-    g_noalloc_addr[dev] = p;
-  }
-  *out = g_noalloc_addr[dev];
+  *out = p;
   return TREE_OK;
 }
 }  // namespace

@@ -95,7 +95,7 @@ int node_pass(const int32_t* parent, const int32_t* node_len, int32_t n, NodePas
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
-  size_t node, tok, cls, rptr, cptr, ridx, cidx, rord, cord, hmin, hmax, runs, nruns, cnt, total;
+  size_t node, tok, cls, rptr, cptr, ridx, cidx, rord, cord, hmin, hmax, runs, nruns, cnt, tcnt, total;
 };
 
 Layout layout(int n, int N, int T) {
@@ -117,6 +117,7 @@ Layout layout(int n, int N, int T) {
   L.runs = o; o += align256((size_t)T * TREE_MAX_RUNS * 16);
   L.nruns = o; o += align256(T * 4);
   L.cnt = o;  o += align256(4 * 4);
+  L.tcnt = o; o += align256(3 * (size_t)T * 4);   // row count, row full, column count
   L.total = o;
   (void)N;
   return L;
@@ -133,51 +134,95 @@ struct PlanDev {
   int pos0;                 // position of the first token of every root (0, or a gateway's length)
 };
 
-// a2: one thread per packed token (padding included).  The token's node is the last node
-// in preorder whose first token is <= t (zero-length nodes share their successor's start).
-__global__ void k_plan_expand(PlanDev P) {
-  const int t = blockIdx.x * blockDim.x + threadIdx.x;
-  const int Np = P.T * TILE;
-  if (t >= Np) return;
+// Sum of `v` over the block (blockDim.x a multiple of 32, at most 1024 threads); every thread
+// gets the result.  `red` is shared scratch of 32 ints; the call ends with a barrier so the
+// scratch may be reused at once.
+__device__ __forceinline__ int block_sum(int v, int* red) {
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  int s = 0;
+  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) s += red[i];
+  __syncthreads();
+  return s;
+}
+
+// Launch 1 (a2 + per key tile data): one block of 128 threads per tile, one thread per packed
+// token (padding included).  A token's node is the last node in preorder whose first token is
+// <= t (zero-length nodes share their successor's start).  The block then reduces the tile's
+// hi range over its real tokens and splits the tile into maximal runs of one node (a run starts
+// where dfs_in changes; padding, dfs_in = -1, is one more run), recording the first
+// TREE_MAX_RUNS runs with their node interval: the attention kernels test the ancestor interval
+// once per run instead of once per token.
+__global__ void __launch_bounds__(TILE) k_plan_tokens(PlanDev P, int32_t* hmin, int32_t* hmax, int32_t* runs,
+                                                      int32_t* nruns) {
+  const int kt = blockIdx.x, c = threadIdx.x;
+  const int t = kt * TILE + c;
+  __shared__ int s_in[TILE], s_out[TILE];
+  __shared__ int s_mn[TILE / 32], s_mx[TILE / 32];
+  __shared__ int starts[TILE + 1];
+  __shared__ int s_nrun;
+  int tin = -1, tout = -2, hi = -1;
   if (t >= P.N) {
     P.tok_node[t] = -1; P.pos[t] = 0; P.g[t] = 0; P.w[t] = 0.f;
     P.tok_in[t] = -1; P.tok_out[t] = -2; P.hi[t] = -1;
-    return;
+  } else {
+    int lo = 0, up = P.n - 1;                 // largest k with dfs_tok_start[k] <= t
+    while (lo < up) {
+      const int mid = (lo + up + 1) >> 1;
+      if (P.dfs_tok_start[mid] <= t) lo = mid; else up = mid - 1;
+    }
+    const int v = P.order[lo];
+    const int gv = P.leaves[v];
+    tin = P.dfs_in[v];
+    tout = P.dfs_out[v];
+    hi = P.sub_end[v] - 1;
+    P.tok_node[t] = v;
+    P.pos[t] = P.pos0 + P.depth_off[v] + (t - P.tok_start[v]);
+    P.g[t] = gv;
+    P.w[t] = __fdiv_rn(static_cast<float>(gv), static_cast<float>(P.K));
+    P.tok_in[t] = tin;
+    P.tok_out[t] = tout;
+    P.hi[t] = hi;
   }
-  int lo = 0, hi = P.n - 1;                 // largest k with dfs_tok_start[k] <= t
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (P.dfs_tok_start[mid] <= t) lo = mid; else hi = mid - 1;
-  }
-  const int v = P.order[lo];
-  const int gv = P.leaves[v];
-  P.tok_node[t] = v;
-  P.pos[t] = P.pos0 + P.depth_off[v] + (t - P.tok_start[v]);
-  P.g[t] = gv;
-  P.w[t] = __fdiv_rn(static_cast<float>(gv), static_cast<float>(P.K));
-  P.tok_in[t] = P.dfs_in[v];
-  P.tok_out[t] = P.dfs_out[v];
-  P.hi[t] = P.sub_end[v] - 1;
-}
-
-// per key tile: min and max of hi over its real tokens
-__global__ void k_tile_hi_range(const int32_t* hi, int N, int32_t* hmin, int32_t* hmax) {
-  const int kt = blockIdx.x;
-  const int j = kt * TILE + threadIdx.x;
-  int mn = 0x7fffffff, mx = -1;
-  if (j < N) { mn = hi[j]; mx = hi[j]; }
+  s_in[c] = tin;
+  s_out[c] = tout;
+  // hi range over the real tokens (none: INT_MAX, -1)
+  int mn = t < P.N ? hi : 0x7fffffff, mx = t < P.N ? hi : -1;
   for (int o = 16; o; o >>= 1) {
     mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
     mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   }
-  __shared__ int smn[TILE / 32], smx[TILE / 32];
-  if ((threadIdx.x & 31) == 0) { smn[threadIdx.x >> 5] = mn; smx[threadIdx.x >> 5] = mx; }
+  if ((c & 31) == 0) { s_mn[c >> 5] = mn; s_mx[c >> 5] = mx; }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int i = 1; i < TILE / 32; ++i) { mn = min(mn, smn[i]); mx = max(mx, smx[i]); }
-    hmin[kt] = mn;
-    hmax[kt] = mx;
+  if (c < 32) {                               // warp 0: range, then the run starts in order
+    const int lane = c;
+    if (lane == 0) {
+      for (int i = 1; i < TILE / 32; ++i) { mn = min(mn, s_mn[i]); mx = max(mx, s_mx[i]); }
+      hmin[kt] = min(mn, s_mn[0]);
+      hmax[kt] = max(mx, s_mx[0]);
+    }
+    int base = 0;
+    for (int ch = 0; ch < TILE / 32; ++ch) {
+      const int cc = ch * 32 + lane;
+      const bool head = (cc == 0) || (s_in[cc] != s_in[cc - 1]);
+      const unsigned m = __ballot_sync(0xffffffffu, head);
+      if (head) starts[base + __popc(m & ((1u << lane) - 1))] = cc;
+      base += __popc(m);
+    }
+    if (lane == 0) { starts[base] = TILE; s_nrun = base; }
   }
+  __syncthreads();
+  const int nr = s_nrun;
+  int32_t* rt = runs + (size_t)kt * TREE_MAX_RUNS * 4;
+  if (c < nr && c < TREE_MAX_RUNS) {
+    const int st = starts[c];
+    rt[4 * c + 0] = st;
+    rt[4 * c + 1] = starts[c + 1];
+    rt[4 * c + 2] = s_in[st];
+    rt[4 * c + 3] = s_out[st];
+  }
+  if (c == 0) nruns[kt] = nr;
 }
 
 // Class of tile (qt, kt).  With hi[j] the last token of node(j)'s subtree, token i sees j
@@ -192,163 +237,93 @@ __device__ __forceinline__ uint8_t tile_class_of(int qt, int kt, int N, const in
   return 1;
 }
 
-// a3: one block per query tile: classes of its row, row count, global tallies
-__global__ void k_tile_rows(int N, int T, const int32_t* hmin, const int32_t* hmax, uint8_t* cls,
-                            int32_t* row_cnt /* row_ptr + 1 */, int32_t* counts) {
-  const int qt = blockIdx.x;
-  int nnz = 0, nfull = 0;
-  for (int kt = threadIdx.x; kt < T; kt += blockDim.x) {
-    const uint8_t c = tile_class_of(qt, kt, N, hmin, hmax);
-    cls[(size_t)qt * T + kt] = c;
-    nnz += (c != 0);
-    nfull += (c == 2);
-  }
-  for (int o = 16; o; o >>= 1) {
-    nnz += __shfl_xor_sync(0xffffffffu, nnz, o);
-    nfull += __shfl_xor_sync(0xffffffffu, nfull, o);
-  }
-  __shared__ int s_nnz[32], s_full[32];
-  const int w = threadIdx.x >> 5;
-  if ((threadIdx.x & 31) == 0) { s_nnz[w] = nnz; s_full[w] = nfull; }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int a = 0, b = 0;
-    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) { a += s_nnz[i]; b += s_full[i]; }
-    row_cnt[qt] = a;
-    atomicAdd(&counts[0], a);
-    atomicAdd(&counts[1], b);
-    atomicAdd(&counts[2], a - b);
-  }
-}
-
-__global__ void k_tile_cols(int N, int T, const int32_t* hmin, const int32_t* hmax,
-                            int32_t* col_cnt /* col_ptr + 1 */) {
-  const int kt = blockIdx.x;
-  int nnz = 0;
-  for (int qt = kt + threadIdx.x; qt < T; qt += blockDim.x) nnz += (tile_class_of(qt, kt, N, hmin, hmax) != 0);
-  for (int o = 16; o; o >>= 1) nnz += __shfl_xor_sync(0xffffffffu, nnz, o);
-  __shared__ int s[32];
-  if ((threadIdx.x & 31) == 0) s[threadIdx.x >> 5] = nnz;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int a = 0;
-    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) a += s[i];
-    col_cnt[kt] = a;
-  }
-}
-
-// single block: counts -> exclusive prefix sums (in place), and heaviest-first orders
-__global__ void k_tile_scan_order(int T, int32_t* row_ptr, int32_t* col_ptr, int32_t* row_order,
-                                  int32_t* col_order, const int32_t* hmax) {
-  __shared__ int carry[2];
-  __shared__ int warp_sum[2][32];
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  // ranks first (needs the raw counts, held in ptr[1..T])
-  // rows: descending count; columns: descending last query tile (hi_max / 128), then
-  // descending count; ties by ascending index
-  for (int i = threadIdx.x; i < T; i += blockDim.x) {
-    const int rc = row_ptr[i + 1], cc = col_ptr[i + 1], cl = hmax[i] / TILE;
-    int rr = 0, cr = 0;
-    for (int j = 0; j < T; ++j) {
-      const int rj = row_ptr[j + 1], cj = col_ptr[j + 1], lj = hmax[j] / TILE;
-      rr += (rj > rc) || (rj == rc && j < i);
-      cr += (lj > cl) || (lj == cl && (cj > cc || (cj == cc && j < i)));
-    }
-    row_order[rr] = i;
-    col_order[cr] = i;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) { carry[0] = 0; carry[1] = 0; row_ptr[0] = 0; col_ptr[0] = 0; }
-  __syncthreads();
-  for (int base = 0; base < T; base += blockDim.x) {
-    const int i = base + threadIdx.x;
-    int a = (i < T) ? row_ptr[i + 1] : 0;
-    int b = (i < T) ? col_ptr[i + 1] : 0;
-    for (int o = 1; o < 32; o <<= 1) {                    // inclusive warp scan
-      const int ya = __shfl_up_sync(0xffffffffu, a, o), yb = __shfl_up_sync(0xffffffffu, b, o);
-      if (lane >= o) { a += ya; b += yb; }
-    }
-    if (lane == 31) { warp_sum[0][w] = a; warp_sum[1][w] = b; }
-    __syncthreads();
-    int pa = carry[0], pb = carry[1];
-    for (int k = 0; k < w; ++k) { pa += warp_sum[0][k]; pb += warp_sum[1][k]; }
-    __syncthreads();
-    if (i < T) { row_ptr[i + 1] = a + pa; col_ptr[i + 1] = b + pb; }
-    if (threadIdx.x == blockDim.x - 1) {
-      int ta_ = carry[0], tb = carry[1];
-      for (int k = 0; k < nw; ++k) { ta_ += warp_sum[0][k]; tb += warp_sum[1][k]; }
-      carry[0] = ta_;
-      carry[1] = tb;
-    }
-    __syncthreads();
-  }
-}
-
-// one block per query tile (rows) or key tile (cols): ordered compaction of non-empty tiles
-__global__ void k_tile_fill(int T, const uint8_t* cls, const int32_t* row_ptr, int32_t* row_idx,
-                            const int32_t* col_ptr, int32_t* col_idx) {
-  const bool cols = blockIdx.y == 1;
+// Launch 2 (a3 classes): block a writes row a of the class table and counts the non-empty and
+// full tiles of row a and the non-empty tiles of column a.
+__global__ void __launch_bounds__(256) k_plan_classes(int N, int T, const int32_t* hmin, const int32_t* hmax,
+                                                      uint8_t* cls, int32_t* row_cnt, int32_t* row_full,
+                                                      int32_t* col_cnt) {
+  __shared__ int red[32];
   const int a = blockIdx.x;
-  int32_t* out = cols ? col_idx + col_ptr[a] : row_idx + row_ptr[a];
-  __shared__ int warp_cnt[32];
-  __shared__ int carry;
-  if (threadIdx.x == 0) carry = 0;
-  __syncthreads();
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int rn = 0, rf = 0, cn = 0;
+  for (int b = threadIdx.x; b < T; b += blockDim.x) {
+    const uint8_t c = tile_class_of(a, b, N, hmin, hmax);
+    cls[(size_t)a * T + b] = c;
+    rn += (c != 0);
+    rf += (c == 2);
+    cn += (tile_class_of(b, a, N, hmin, hmax) != 0);
+  }
+  rn = block_sum(rn, red);
+  rf = block_sum(rf, red);
+  cn = block_sum(cn, red);
+  if (threadIdx.x == 0) { row_cnt[a] = rn; row_full[a] = rf; col_cnt[a] = cn; }
+}
+
+// Launch 3 (a3 CSR and orders): block a computes, from the per-row / per-column counts of
+// launch 2, the offsets row_ptr[a], col_ptr[a] (sums over the rows / columns before a), the
+// ranks of row a and column a in the heaviest-first orders (rows: count descending, then index;
+// columns: last non-empty query tile descending, then count descending, then index), and
+// fills row a's and column a's lists in ascending order.  The last block writes the totals.
+__global__ void __launch_bounds__(256) k_plan_lists(int N, int T, const int32_t* hmin, const int32_t* hmax,
+                                                    const int32_t* row_cnt, const int32_t* row_full,
+                                                    const int32_t* col_cnt, int32_t* row_ptr, int32_t* row_idx,
+                                                    int32_t* col_ptr, int32_t* col_idx, int32_t* row_order,
+                                                    int32_t* col_order, int32_t* counts) {
+  __shared__ int red[32];
+  __shared__ int wrow[32], wcol[32];
+  const int a = blockIdx.x;
+  const int ra = row_cnt[a], ca = col_cnt[a], la = hmax[a] / TILE;
+  int pr = 0, pc = 0, rr = 0, cr = 0, tf = 0;
+  for (int j = threadIdx.x; j < T; j += blockDim.x) {
+    const int rj = row_cnt[j], cj = col_cnt[j], lj = hmax[j] / TILE;
+    if (j < a) { pr += rj; pc += cj; }
+    rr += (rj > ra) || (rj == ra && j < a);
+    cr += (lj > la) || (lj == la && (cj > ca || (cj == ca && j < a)));
+    tf += row_full[j];
+  }
+  pr = block_sum(pr, red);
+  pc = block_sum(pc, red);
+  rr = block_sum(rr, red);
+  cr = block_sum(cr, red);
+  if (threadIdx.x == 0) {
+    row_ptr[a] = pr;
+    col_ptr[a] = pc;
+    row_order[rr] = a;
+    col_order[cr] = a;
+  }
+  if (a == T - 1) {
+    tf = block_sum(tf, red);
+    if (threadIdx.x == 0) {
+      row_ptr[T] = pr + ra;
+      col_ptr[T] = pc + ca;
+      counts[0] = pr + ra;
+      counts[1] = tf;
+      counts[2] = pr + ra - tf;
+      counts[3] = 0;
+    }
+  }
+  // ordered compaction of the non-empty tiles of row a (over kt) and column a (over qt)
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int orow = pr, ocol = pc;
   for (int base = 0; base < T; base += blockDim.x) {
     const int b = base + threadIdx.x;
-    bool nz = false;
-    if (b < T) nz = cols ? cls[(size_t)b * T + a] != 0 : cls[(size_t)a * T + b] != 0;
-    const unsigned m = __ballot_sync(0xffffffffu, nz);
-    if (lane == 0) warp_cnt[w] = __popc(m);
+    const bool nr = b < T && tile_class_of(a, b, N, hmin, hmax) != 0;
+    const bool nc = b < T && tile_class_of(b, a, N, hmin, hmax) != 0;
+    const unsigned mr = __ballot_sync(0xffffffffu, nr), mc = __ballot_sync(0xffffffffu, nc);
+    if (lane == 0) { wrow[w] = __popc(mr); wcol[w] = __popc(mc); }
     __syncthreads();
-    int off = carry;
-    for (int k = 0; k < w; ++k) off += warp_cnt[k];
-    if (nz) out[off + __popc(m & ((1u << lane) - 1))] = b;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      int s = carry;
-      for (int k = 0; k < (int)(blockDim.x >> 5); ++k) s += warp_cnt[k];
-      carry = s;
+    int offr = orow, offc = ocol, totr = 0, totc = 0;
+    for (int k = 0; k < nw; ++k) {
+      if (k < w) { offr += wrow[k]; offc += wcol[k]; }
+      totr += wrow[k];
+      totc += wcol[k];
     }
+    const unsigned below = (1u << lane) - 1;
+    if (nr) row_idx[offr + __popc(mr & below)] = b;
+    if (nc) col_idx[offc + __popc(mc & below)] = b;
+    orow += totr;
+    ocol += totc;
     __syncthreads();
   }
-}
-
-// One warp per tile: split the tile's 128 tokens into maximal runs of one node (a run starts
-// where dfs_in changes; padding, dfs_in = -1, is one more run) and record the first
-// TREE_MAX_RUNS of them with their node interval.  The kernels test the ancestor interval once
-// per run instead of once per token.
-__global__ void k_tile_runs(const int32_t* tok_in, const int32_t* tok_out, int32_t* runs, int32_t* nruns) {
-  const int t = blockIdx.x, lane = threadIdx.x;
-  const int32_t* in = tok_in + (size_t)t * TILE;
-  const int32_t* out = tok_out + (size_t)t * TILE;
-  int32_t* rt = runs + (size_t)t * TREE_MAX_RUNS * 4;
-  __shared__ int starts[TILE + 1];
-  int base = 0;
-  for (int ch = 0; ch < TILE / 32; ++ch) {
-    const int c = ch * 32 + lane;
-    const bool head = (c == 0) || (in[c] != in[c - 1]);
-    const unsigned m = __ballot_sync(0xffffffffu, head);
-    if (head) starts[base + __popc(m & ((1u << lane) - 1))] = c;
-    base += __popc(m);
-  }
-  __syncwarp();
-  if (lane == 0) starts[base] = TILE;
-  __syncwarp();
-  for (int k = lane; k < base && k < TREE_MAX_RUNS; k += 32) {
-    const int st = starts[k];
-    rt[4 * k + 0] = st;
-    rt[4 * k + 1] = starts[k + 1];
-    rt[4 * k + 2] = in[st];
-    rt[4 * k + 3] = out[st];
-  }
-  if (lane == 0) nruns[t] = base;
-}
-
-__global__ void k_zero_i32(int32_t* p, int n) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < n) p[i] = 0;
 }
 
 }  // namespace
@@ -369,6 +344,15 @@ int tree_plan_query(const int32_t* parent, const int32_t* node_len, int32_t n_no
   info->n_paths = np.K;
   info->max_nnz = (int64_t)np.T * (np.T + 1) / 2;
   info->plan_bytes = (int64_t)layout(np.n, np.N, np.T).total;
+  return TREE_OK;
+}
+
+int tree_plan_nodes(const int32_t* parent, const int32_t* node_len, int32_t n_nodes, int32_t* out) {
+  if (!out) return TREE_ERR_ARG;
+  NodePass np;
+  const int rc = node_pass(parent, node_len, n_nodes, &np);
+  if (rc) return rc;
+  std::memcpy(out, np.block.data(), np.block.size() * sizeof(int32_t));
   return TREE_OK;
 }
 
@@ -429,15 +413,16 @@ int tree_plan_offset(const int32_t* parent, const int32_t* node_len, int32_t n_n
   if (rc) return rc;
   PlanDev P{p->order, p->dfs_in, p->dfs_out, p->tok_start, p->depth_off, p->leaves, p->dfs_tok_start,
             p->sub_end, p->tok_node, p->pos, p->g, p->tok_in, p->tok_out, p->hi, p->w, n, N, T, np.K, pos_offset};
-  const int Np = T * TILE;
-  k_plan_expand<<<(Np + 255) / 256, 256, 0, s>>>(P);
-  k_zero_i32<<<1, 32, 0, s>>>(p->counts, 4);
-  k_tile_hi_range<<<T, TILE, 0, s>>>(p->hi, N, p->tile_hi_min, p->tile_hi_max);
-  k_tile_runs<<<T, 32, 0, s>>>(p->tok_in, p->tok_out, p->tile_runs, p->tile_nruns);
-  k_tile_rows<<<T, 256, 0, s>>>(N, T, p->tile_hi_min, p->tile_hi_max, p->tile_class, p->row_ptr + 1, p->counts);
-  k_tile_cols<<<T, 256, 0, s>>>(N, T, p->tile_hi_min, p->tile_hi_max, p->col_ptr + 1);
-  k_tile_scan_order<<<1, 1024, 0, s>>>(T, p->row_ptr, p->col_ptr, p->row_order, p->col_order, p->tile_hi_max);
-  k_tile_fill<<<dim3(T, 2), 256, 0, s>>>(T, p->tile_class, p->row_ptr, p->row_idx, p->col_ptr, p->col_idx);
+  // Three launches: tokens and per-key-tile data; classes and per-row / per-column counts; CSR
+  // lists and orders.  The counts go to the scratch tree_plan_bind() lays out right after the
+  // `counts` words (3 T int32: row count, row full count, column count).
+  const Layout L = layout(n, N, T);
+  int32_t* tcnt = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(p->counts) + (L.tcnt - L.cnt));
+  k_plan_tokens<<<T, TILE, 0, s>>>(P, p->tile_hi_min, p->tile_hi_max, p->tile_runs, p->tile_nruns);
+  k_plan_classes<<<T, 256, 0, s>>>(N, T, p->tile_hi_min, p->tile_hi_max, p->tile_class, tcnt, tcnt + T,
+                                   tcnt + 2 * T);
+  k_plan_lists<<<T, 256, 0, s>>>(N, T, p->tile_hi_min, p->tile_hi_max, tcnt, tcnt + T, tcnt + 2 * T, p->row_ptr,
+                                 p->row_idx, p->col_ptr, p->col_idx, p->row_order, p->col_order, p->counts);
   return record_cuda(cudaGetLastError());
 }
 

@@ -5,8 +5,8 @@ except the subtrees of cut's children, and each child of cut roots one child par
 child partitions read the K/V of the path root..cut (the gateway) from the parent partition
 instead of recomputing it, and their gradients w.r.t. the gateway are relayed back to it.
 
-This module only renumbers nodes and tokens (depth-first packing with children by ascending id,
-the same order the plan uses); the attention itself runs in the library.
+This module only renumbers nodes and tokens; the packed token starts come from the library's
+own host plan pass (tree_plan_nodes), and the attention itself runs in the library.
 """
 from __future__ import annotations
 
@@ -25,23 +25,10 @@ class Partition:
 
 
 def packed_starts(parent, node_len):
-    """First packed token of every node: depth-first preorder, roots and children by ascending id."""
-    parent = np.asarray(parent, dtype=np.int64)
-    node_len = np.asarray(node_len, dtype=np.int64)
-    kids = [[] for _ in range(len(parent))]
-    roots = []
-    for v, p in enumerate(parent):
-        (roots if p < 0 else kids[p]).append(v)
-    start = np.zeros(len(parent), dtype=np.int64)
-    tok = 0
-    for r in roots:
-        stack = [r]
-        while stack:
-            v = stack.pop()
-            start[v] = tok
-            tok += node_len[v]
-            stack.extend(reversed(kids[v]))       # ascending ids leave the stack in order
-    return start
+    """First packed token of every node, from the library's host plan pass (depth-first
+    preorder, roots and children by ascending id)."""
+    from . import tree_plan_nodes
+    return tree_plan_nodes(parent, node_len)["tok_start"]
 
 
 def _subtree(kids, v):

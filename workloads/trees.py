@@ -128,21 +128,27 @@ def rollout_tree(seed: int = 0, root_len: int = 2048, depth: int = 5, branch=(2,
 
 
 def ffd_pack(lengths, row_tokens):
-    """First-fit-decreasing: longest first, each into the first row with room; returns rows of indices."""
-    order = sorted(range(len(lengths)), key=lambda i: (-lengths[i], i))
-    rows, used = [], []
-    for i in order:
-        n = lengths[i]
-        if n > row_tokens:
-            raise ValueError(f"sequence of {n} tokens exceeds a row of {row_tokens}")
-        r = next((r for r, u in enumerate(used) if u + n <= row_tokens), None)
-        if r is None:
-            rows.append([])
-            used.append(0)
-            r = len(rows) - 1
-        rows[r].append(i)
-        used[r] += n
-    return rows
+    """First-fit-decreasing bin packing: items are placed longest first (ties: lower index), each
+    into the lowest-numbered row whose remaining room holds it, a new row opened when none does.
+    Returns, per row, the item indices in placement order."""
+    lengths = np.asarray(lengths, dtype=np.int64)
+    too_long = np.flatnonzero(lengths > row_tokens)
+    if too_long.size:
+        raise ValueError(f"item {int(too_long[0])} ({int(lengths[too_long[0]])} tokens) does not fit a row of "
+                         f"{row_tokens}")
+    placement = np.lexsort((np.arange(lengths.size), -lengths))     # primary key: length, descending
+    room = np.zeros(0, dtype=np.int64)                              # remaining capacity per open row
+    row_of = np.empty(lengths.size, dtype=np.int64)
+    for item in placement:
+        fits = np.flatnonzero(room >= lengths[item])
+        if fits.size == 0:
+            room = np.append(room, row_tokens)
+            target = room.size - 1
+        else:
+            target = int(fits[0])
+        room[target] -= lengths[item]
+        row_of[item] = target
+    return [[int(i) for i in placement if row_of[i] == r] for r in range(room.size)]
 
 
 def forest_tree(seed: int = 0, row_tokens: int = 16384, n_rows: int = 8, median: float = 1024.0,
