@@ -183,6 +183,13 @@ def run_ours(args, rank, world, dev):
     st = host_stats(wl.parent, wl.node_len)
     t = make_tensors(wl)
     Hq, Hkv, d, N = wl.Hq, wl.Hkv, wl.d, st["N"]
+    if args.shard == "heads":
+        # this rank's kv-head group(s) of the one tree: its q / k / v / u heads, the whole plan
+        from tree_masked_attention_plan_gb300.shard import kv_head_shard
+        sh = kv_head_shard(Hq, Hkv, rank, world)
+        t = {"q": t["q"][:, sh.q0:sh.q1].contiguous(), "k": t["k"][:, sh.kv0:sh.kv1].contiguous(),
+             "v": t["v"][:, sh.kv0:sh.kv1].contiguous(), "u": t["u"][:, sh.q0:sh.q1].contiguous()}
+        Hq, Hkv = sh.Hq, sh.Hkv
     stream = torch.cuda.current_stream()
     q, k, v, u = (t[x].to(dev) for x in ("q", "k", "v", "u"))
     status = tam.new_status(dev)
@@ -195,12 +202,14 @@ def run_ours(args, rank, world, dev):
     ws = torch.empty(tam.tree_attn_bwd_workspace(plan, Hq, d), dtype=torch.uint8, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    ev = {n: [torch.cuda.Event(enable_timing=True) for _ in range(2)] for n in ("step", "fwd")}
+    ev = {n: [torch.cuda.Event(enable_timing=True) for _ in range(2)] for n in ("step", "fwd", "plan", "rope")}
     bwd_ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     theta = wl.theta
 
     def step(p):
+        ev["rope"][0].record(stream)
         tam.tree_rope_fwd(p, q, k, theta, qr=qr, kr=kr)
+        ev["rope"][1].record(stream)
         ev["fwd"][0].record(stream)
         tam.tree_attn_fwd(p, qr, kr, v, o=o, lse=lse, status=status)
         ev["fwd"][1].record(stream)
@@ -210,7 +219,9 @@ def run_ours(args, rank, world, dev):
 
     def full_step():
         ev["step"][0].record(stream)
+        ev["plan"][0].record(stream)
         p = tam.tree_plan(wl.parent, wl.node_len, device=dev)
+        ev["plan"][1].record(stream)
         step(p)
         ev["step"][1].record(stream)
         return p
@@ -221,7 +232,7 @@ def run_ours(args, rank, world, dev):
         full_step()
     torch.cuda.synchronize()
     tam.check_status(status, "warmup")
-    times = {"step": [], "fwd": [], "bwd": [], "dkdv": []}
+    times = {"step": [], "fwd": [], "bwd": [], "dkdv": [], "plan": [], "rope": []}
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -233,6 +244,8 @@ def run_ours(args, rank, world, dev):
             torch.cuda.synchronize()
             times["step"].append(ev["step"][0].elapsed_time(ev["step"][1]))
             times["fwd"].append(ev["fwd"][0].elapsed_time(ev["fwd"][1]))
+            times["plan"].append(ev["plan"][0].elapsed_time(ev["plan"][1]))
+            times["rope"].append(ev["rope"][0].elapsed_time(ev["rope"][1]))
             times["bwd"].append(bwd_ev[0].elapsed_time(bwd_ev[3]))
             times["dkdv"].append(bwd_ev[1].elapsed_time(bwd_ev[2]))
         torch.cuda.synchronize()
@@ -243,6 +256,11 @@ def run_ours(args, rank, world, dev):
     tam.check_status(status, "timed steps")
     clocks = clk.summary()
 
+    res = dict(st=st, wl=wl, times=times, wall=wall, clocks=clocks, e2e_ms=float("nan"), h2d=0, d2h=0,
+               nnz=int(plan.arrays()["counts"][0].item()), Hq_local=Hq, Hkv_local=Hkv, T=plan.n_tiles,
+               n_nodes=len(wl.parent))
+    if args.no_e2e:
+        return res
     # e2e: the same step through the public API from pinned host buffers; every step copies its
     # inputs in and its outputs out.  As a training input pipeline does, step i+1's inputs are
     # copied in and step i's outputs copied out on side streams while the next step computes
@@ -317,8 +335,7 @@ def run_ours(args, rank, world, dev):
         if not torch.equal(got.to(dev), ref):
             raise RuntimeError(f"e2e pipeline: {name} differs from the device-timed step's")
 
-    res = dict(st=st, wl=wl, times=times, wall=wall, clocks=clocks, e2e_ms=float(np.mean(e2e_ms)), h2d=h2d, d2h=d2h,
-               nnz=int(plan.arrays()["counts"][0].item()))
+    res.update(e2e_ms=float(np.mean(e2e_ms)), h2d=h2d, d2h=d2h)
     return res
 
 
@@ -636,18 +653,21 @@ def ce_cpu_baseline(wl, h, W, labels, budget_s=15.0):
 
 def cpu_baseline_sample(config, budget_s=20.0):
     """The oracle as it stands, on the host cores: path-expanded fp64 attention fwd+bwd for q head 0
-    over a prefix of the root-to-leaf paths that fits the time budget.  Credit: 14 d times the
-    visible pairs the sampled paths compute (each path is its own causal sequence)."""
+    over a prefix of the root-to-leaf paths that fits the time budget.  Reported on the GPU line's
+    metric: the sample's time is scaled to every path (by the path-expanded causal pairs they
+    compute) and every q head, and the whole tree's 14 d Hq N_pairs unique visible-pair flops are
+    divided by that time."""
     import oracle
     wl = make_workload(config)
     t = make_tensors(wl)
     p = oracle.plan(wl.parent, wl.node_len)
+    path_len = [int(sum(wl.node_len[x] for x in path)) for path in p["paths"]]
+    all_path_pairs = sum(L * (L + 1) // 2 for L in path_len)
     done_pairs, t0, n_paths = 0, time.perf_counter(), 0
     sub = dict(p)
-    for path in p["paths"]:
+    for path, L in zip(p["paths"], path_len):
         sub["paths"] = [path]
         sub["n_paths"] = p["n_paths"]
-        L = int(sum(wl.node_len[x] for x in path))
         oracle.attention_paths(wl.parent, wl.node_len, t["q"][:, :1], t["k"][:, :1], t["v"][:, :1], t["u"][:, :1],
                                heads=[0], p=sub, theta=wl.theta)
         done_pairs += L * (L + 1) // 2
@@ -655,10 +675,14 @@ def cpu_baseline_sample(config, budget_s=20.0):
         if time.perf_counter() - t0 > budget_s:
             break
     el = time.perf_counter() - t0
+    whole_tree_s = el * (all_path_pairs / done_pairs) * wl.Hq      # every path, every q head
+    n_pairs = host_stats(wl.parent, wl.node_len)["n_pairs"]
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    return dict(value=14 * wl.d * done_pairs / el / 1e12, unit=UNIT, cores=cores, kind="oracle",
+    return dict(value=14 * wl.d * wl.Hq * n_pairs / whole_tree_s / 1e12, unit=UNIT, cores=cores, kind="oracle",
                 sample=f"{config}: fp64 path-expanded fwd+bwd, q head 0, first {n_paths} of {p['n_paths']} "
-                       f"root-to-leaf paths ({done_pairs} causal pairs), {el:.1f} s; NumPy/BLAS default threads",
+                       f"root-to-leaf paths ({done_pairs} of {all_path_pairs} path-expanded causal pairs) in {el:.1f} s; "
+                       f"scaled to all paths and {wl.Hq} q heads ({whole_tree_s:.0f} s) and credited the tree's "
+                       f"unique visible-pair flops 14 d Hq N_pairs; NumPy/BLAS default threads",
                 seconds=el)
 
 
@@ -670,6 +694,8 @@ def main():
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=list(CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the end-to-end (host buffers) leg, e.g. under a profiler")
     ap.add_argument("--conv", action="store_true",
                     help="time the hybrid-layer tree convolution (forward + backward) instead of attention")
     ap.add_argument("--ce", action="store_true",
@@ -679,6 +705,9 @@ def main():
     ap.add_argument("--ce-chunk", type=int, default=8192)
     ap.add_argument("--conv-channels", type=int, default=8192)
     ap.add_argument("--conv-k", type=int, default=4)
+    ap.add_argument("--shard", default="trees", choices=["trees", "heads"],
+                    help="multi-rank split: 'trees' = one tree per rank (weak scaling); 'heads' = one tree "
+                         "split by kv-head groups, plan replicated, no exchange (strong scaling)")
     ap.add_argument("--partition", action="store_true",
                     help="run the tree as gateway partitions (parent + children of the largest cut)")
     args = ap.parse_args()
@@ -732,27 +761,48 @@ def main():
     ms = float(np.mean(times["step"]))
     ms_fwd, ms_bwd, ms_dkdv = (float(np.mean(times[x])) for x in ("fwd", "bwd", "dkdv"))
     ms_max, e2e_max = reduce_max([ms, res["e2e_ms"]], dev, world)
-    flops = 14.0 * wl.d * wl.Hq * st["n_pairs"]
+    flops = 14.0 * wl.d * wl.Hq * st["n_pairs"]            # the whole tree, all heads
     peaks = load_peaks()
-    value = world * flops / (ms_max * 1e-3) / 1e12
-    dkdv_flops = 10.0 * wl.d * wl.Hq * st["n_pairs"]
+    heads = args.shard == "heads"
+    trees = 1 if heads else world                           # trees the job processes per step
+    value = trees * flops / (ms_max * 1e-3) / 1e12
+    dkdv_flops = 10.0 * wl.d * res["Hq_local"] * st["n_pairs"]    # this rank's heads
     achieved = dkdv_flops / (ms_dkdv * 1e-3) / 1e12
+    ms_plan, ms_rope = (float(np.mean(times[x])) for x in ("plan", "rope"))
+    hq_l, hkv_l, T = res["Hq_local"], res["Hkv_local"], res["T"]
+    # algorithmic bytes: RoPE reads and writes q, k (bf16) and reads pos; the plan writes 7 int32 /
+    # fp32 arrays per padded token, the T x T class table, both CSR index lists and the node block
+    rope_bytes = st["N"] * (2 * (hq_l + hkv_l) * wl.d * 2 + 4)
+    plan_bytes = 28 * T * 128 + T * T + 8 * res["nnz"] + 32 * res["n_nodes"]
+    local_pairs_flops = wl.d * hq_l * st["n_pairs"]
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
+            "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "higher_is_better": True,
+            "scaling": "strong" if heads else "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded tree and N(0,1) bf16 tensors)",
             "config": {"workload": wl.name, "N": st["N"], "paths_K": st["K"], "N_pairs": st["n_pairs"],
                        "N_flat": st["n_flat"], "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d, "rope_theta": wl.theta,
                        "nonempty_tiles": res["nnz"], "step": "plan+rope+fwd+weights+bwd",
                        "l2": "flushed between steps (256 MiB write, outside the event brackets)",
-                       "parallelism": f"one tree per rank x{world}"},
-            "tokens_per_s": round(world * st["N"] / (ms_max * 1e-3), 1),
+                       "parallelism": (f"one tree split by kv-head groups over {world} ranks (plan replicated, "
+                                       f"no data-path exchange)") if heads else f"one tree per rank x{world}"},
+            "tokens_per_s": round(trees * st["N"] / (ms_max * 1e-3), 1),
             "pct_bf16_peak": round(100 * value / world / peaks["bf16"], 2),
-            "breakdown_ms": {"step": round(ms, 4), "fwd": round(ms_fwd, 4), "bwd": round(ms_bwd, 4),
-                             "bwd_dkdv": round(ms_dkdv, 4),
-                             "attention_fwd_bwd_tflops": round(flops / ((ms_fwd + ms_bwd) * 1e-3) / 1e12, 2)},
-            "e2e": {"value": round(world * flops / (e2e_max * 1e-3) / 1e12, 2), "unit": UNIT,
+            "breakdown_ms": {"step": round(ms, 4), "plan": round(ms_plan, 4), "rope": round(ms_rope, 4),
+                             "fwd": round(ms_fwd, 4), "bwd": round(ms_bwd, 4), "bwd_dkdv": round(ms_dkdv, 4),
+                             "attention_fwd_bwd_tflops": round(14 * local_pairs_flops / ((ms_fwd + ms_bwd) * 1e-3)
+                                                               / 1e12, 2)},
+            "fwd_tflops": round(4 * local_pairs_flops / (ms_fwd * 1e-3) / 1e12, 2),
+            "bwd_tflops": round(10 * local_pairs_flops / (ms_bwd * 1e-3) / 1e12, 2),
+            "computed_tile_tflops": round(14.0 * wl.d * hq_l * res["nnz"] * 128 * 128 / ((ms_fwd + ms_bwd) * 1e-3)
+                                          / 1e12, 2),
+            "por": round(1.0 - st["N"] / st["n_flat"], 4),
+            "rope_gbs": round(rope_bytes / (ms_rope * 1e-3) / 1e9, 1),
+            "plan_gbs": round(plan_bytes / (ms_plan * 1e-3) / 1e9, 1),
+            "plan_note": "plan_gbs: algorithmic bytes over the span of tree_plan on the stream (host node pass, one "
+                         "node-block copy, three launches)",
+            "e2e": None if args.no_e2e else {"value": round(trees * flops / (e2e_max * 1e-3) / 1e12, 2), "unit": UNIT,
                     "ms_per_step": round(e2e_max, 4), "h2d_bytes_per_step": res["h2d"],
                     "d2h_bytes_per_step": res["d2h"],
                     "overlap": "step i+1's copy-in and step i's copy-out on side streams during compute"},

@@ -5,8 +5,11 @@
 // One CTA computes one query tile for NH q heads that read the same kv head (NH = 2 when the
 // GQA group size is even, else 1), walking the non-empty key tiles of the tile's row.  Each
 // K/V tile is loaded once for both heads.
-//   warp 0        TMA producer: the NH Q tiles once, then K/V tiles (plus the key tile's
-//                 dfs_in/dfs_out words) into a 2-stage ring;
+//   warps 0, 2    TMA producers: warp 0 the NH Q tiles once, then K tiles into a 2-stage ring;
+//                 warp 2 the V tiles (with the key tile's dfs_in/dfs_out words and node runs)
+//                 into another.  A K stage is free as soon as every head's S MMA has read it, a
+//                 V stage only after the last P V, so the next K tile starts loading a step
+//                 earlier than with one ring for both;
 //   warp 1        allocates TMEM and issues every tcgen05.mma from one thread, head-interleaved:
 //                 O_i += P_i V(n-1), then S_i = Q_i K(n)^T, for i = 0..NH-1;
 //   warps 4+4i..  softmax warpgroup i (head i): thread r owns query row r (TMEM lane r), so the
@@ -40,11 +43,11 @@ struct FwdCfg {
   static constexpr int LIST_OFF = RUNS_OFF + NS * TREE_MAX_RUNS * 16;   // int32 key tiles of the row
   static constexpr int LCLS_OFF = LIST_OFF + kMaxList * 4;     // uint8 their tile classes
   static constexpr int BAR_OFF = LCLS_OFF + kMaxList;
-  static constexpr int NBAR = 1 + 2 * NS + 3 * NH + 1;  // q, kv full/empty, s/p/o per head, drain
+  static constexpr int NBAR = 1 + 4 * NS + 3 * NH + 1;  // q, k and v full/empty, s/p/o per head, drain
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int SMEM = MISC_OFF + 16;
   static constexpr int SMEM_ALLOC = SMEM + 1024;      // slack for 1024-byte alignment
-  // warpgroup 0: producer (warp 0), MMA issuer (warp 1), two idle warps; then one softmax
+  // warpgroup 0: K producer (warp 0), MMA issuer (warp 1), V producer (warp 2), one idle warp; then one softmax
   // warpgroup per head.  With two heads the softmax warpgroups take registers from warpgroup 0.
   static constexpr int THREADS = 128 + NH * 128;
   static constexpr int LAUNCH_REGS = 168;             // 384 x 168 = 64512 (two heads)
@@ -57,8 +60,9 @@ struct FwdCfg {
   static constexpr uint32_t TMEM_COLS = TMEM_NEED <= 256 ? 256 : 512;
   static constexpr uint32_t IDESC_S = idesc_bf16(TILE, TILE, 0, 0);   // Q K-major, K K-major
   static constexpr uint32_t IDESC_PV = idesc_bf16(TILE, HD, 0, 1);    // P (TMEM) K-major, V MN-major
-  static constexpr uint32_t KV_TX = 2 * NCH * CHUNK_BYTES + 2 * TILE * 4 + TREE_MAX_RUNS * 16;
-  static constexpr uint32_t KVG_TX = 2 * NCH * CHUNK_BYTES;           // a gateway tile: K, V only
+  static constexpr uint32_t K_TX = NCH * CHUNK_BYTES;
+  static constexpr uint32_t V_TX = NCH * CHUNK_BYTES + 2 * TILE * 4 + TREE_MAX_RUNS * 16;   // V + mask data
+  static constexpr uint32_t VG_TX = NCH * CHUNK_BYTES;                // a gateway tile: V only
   static constexpr float RESCALE_THRESHOLD = 8.f;     // log2 units
 };
 
@@ -104,9 +108,11 @@ __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
   uint8_t* sm = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::BAR_OFF);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;
-  uint64_t* kv_empty = bars + 1 + C::NS;
-  uint64_t* s_full = bars + 1 + 2 * C::NS;            // [NH] S_i(n) computed (and PV_i(n-1) done)
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = bars + 1 + C::NS;
+  uint64_t* v_full = bars + 1 + 2 * C::NS;            // V tile with the key tile's mask data
+  uint64_t* v_empty = bars + 1 + 3 * C::NS;
+  uint64_t* s_full = bars + 1 + 4 * C::NS;            // [NH] S_i(n) computed (and PV_i(n-1) done)
   uint64_t* p_full = s_full + NH;                     // [NH] P_i(n) in TMEM, O_i rescaled
   uint64_t* o_done = p_full + NH;                     // [NH] last PV_i done
   uint64_t* drain = o_done + NH;
@@ -142,7 +148,12 @@ __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < C::NS; ++s) { mbar_init(&kv_full[s], 1); mbar_init(&kv_empty[s], 1); }
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
     for (int i = 0; i < NH; ++i) { mbar_init(&s_full[i], 1); mbar_init(&p_full[i], 4); mbar_init(&o_done[i], 1); }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -161,52 +172,61 @@ __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
   if (warp < 4) {
     if constexpr (NH == 2) regs_dec<C::REGS_CTRL>();
   if (warp == 0) {
-    // ---------------------------------------------------------------- TMA producer
+    // ---------------------------------------------------------------- TMA producer: Q, K
     if (lane == 0) {
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
-      prefetch_tmap(&tmV);
-      if (GW) {
-        prefetch_tmap(&tmKg);
-        prefetch_tmap(&tmVg);
-      }
+      if (GW) prefetch_tmap(&tmKg);
       mbar_expect_tx(q_full, NH * C::NCH * CHUNK_BYTES);
       for (int i = 0; i < NH; ++i)
         for (int c = 0; c < C::NCH; ++c)
           tma_load_3d(sm + C::Q_OFF + (i * C::NCH + c) * CHUNK_BYTES, &tmQ, q_full, c * 64, h0 + i, qt * TILE);
+      // K(n) waits only for the S MMAs of tile n-2 (k_empty), not for its P V MMAs
       int issued = 0;
       for (int n = 0; n < cnt; ++n) {
         const int s = n % C::NS;
-        if (n >= C::NS && !mbar_wait(&kv_empty[s], ((n / C::NS) - 1) & 1, wc)) break;
         int kt, cls;
         row_tile(n, kt, cls);
-        uint8_t* kb = sm + C::K_OFF + s * C::NCH * CHUNK_BYTES;
-        uint8_t* vb = sm + C::V_OFF + s * C::NCH * CHUNK_BYTES;
-        if (GW && n < G) {                     // gateway tile: K, V only (rows past gw_len read as 0)
-          mbar_expect_tx(&kv_full[s], C::KVG_TX);
-          for (int c = 0; c < C::NCH; ++c) {
-            tma_load_3d(kb + c * CHUNK_BYTES, &tmKg, &kv_full[s], c * 64, kvh, kt * TILE);
-            tma_load_3d(vb + c * CHUNK_BYTES, &tmVg, &kv_full[s], c * 64, kvh, kt * TILE);
-          }
-          issued = n + 1;
-          continue;
-        }
-        mbar_expect_tx(&kv_full[s], C::KV_TX);
-        for (int c = 0; c < C::NCH; ++c) {
-          tma_load_3d(kb + c * CHUNK_BYTES, &tmK, &kv_full[s], c * 64, kvh, kt * TILE);
-          tma_load_3d(vb + c * CHUNK_BYTES, &tmV, &kv_full[s], c * 64, kvh, kt * TILE);
-        }
-        bulk_load(kin_s + s * TILE, p.tok_in + (size_t)kt * TILE, TILE * 4, &kv_full[s]);
-        bulk_load(kout_s + s * TILE, p.tok_out + (size_t)kt * TILE, TILE * 4, &kv_full[s]);
-        bulk_load(sm + C::RUNS_OFF + s * TREE_MAX_RUNS * 16, p.tile_runs + (size_t)kt * TREE_MAX_RUNS * 4,
-                  TREE_MAX_RUNS * 16, &kv_full[s]);
+        if (n >= C::NS && !mbar_wait(&k_empty[s], ((n / C::NS) - 1) & 1, wc)) break;
+        mbar_expect_tx(&k_full[s], C::K_TX);
+        for (int c = 0; c < C::NCH; ++c)          // gateway tile rows past gw_len read as 0
+          tma_load_3d(sm + C::K_OFF + (s * C::NCH + c) * CHUNK_BYTES, (GW && n < G) ? &tmKg : &tmK, &k_full[s],
+                      c * 64, kvh, kt * TILE);
         issued = n + 1;
       }
       if (*abort_flag) {                       // let copies in flight land before exit
         mbar_wait_drain(q_full, 0, p.wait_ns);
         for (int n = (issued > C::NS ? issued - C::NS : 0); n < issued; ++n)
-          mbar_wait_drain(&kv_full[n % C::NS], (n / C::NS) & 1, p.wait_ns);
+          mbar_wait_drain(&k_full[n % C::NS], (n / C::NS) & 1, p.wait_ns);
       }
+    }
+  } else if (warp == 2) {
+    // ---------------------------------------------------------------- TMA producer: V + mask data
+    if (lane == 0) {
+      prefetch_tmap(&tmV);
+      if (GW) prefetch_tmap(&tmVg);
+      int issued = 0;
+      for (int n = 0; n < cnt; ++n) {
+        const int s = n % C::NS;
+        int kt, cls;
+        row_tile(n, kt, cls);
+        const bool gwt = GW && n < G;
+        if (n >= C::NS && !mbar_wait(&v_empty[s], ((n / C::NS) - 1) & 1, wc)) break;
+        mbar_expect_tx(&v_full[s], gwt ? C::VG_TX : C::V_TX);
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_3d(sm + C::V_OFF + (s * C::NCH + c) * CHUNK_BYTES, gwt ? &tmVg : &tmV, &v_full[s], c * 64, kvh,
+                      kt * TILE);
+        if (!gwt) {
+          bulk_load(kin_s + s * TILE, p.tok_in + (size_t)kt * TILE, TILE * 4, &v_full[s]);
+          bulk_load(kout_s + s * TILE, p.tok_out + (size_t)kt * TILE, TILE * 4, &v_full[s]);
+          bulk_load(sm + C::RUNS_OFF + s * TREE_MAX_RUNS * 16, p.tile_runs + (size_t)kt * TREE_MAX_RUNS * 4,
+                    TREE_MAX_RUNS * 16, &v_full[s]);
+        }
+        issued = n + 1;
+      }
+      if (*abort_flag)
+        for (int n = (issued > C::NS ? issued - C::NS : 0); n < issued; ++n)
+          mbar_wait_drain(&v_full[n % C::NS], (n / C::NS) & 1, p.wait_ns);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
@@ -233,27 +253,32 @@ __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
                            (m > 0 || kk > 0) ? 1u : 0u);
         return true;
       };
-      bool ok = mbar_wait(q_full, 0, wc) && (cnt == 0 || mbar_wait(&kv_full[0], 0, wc));
+      bool ok = mbar_wait(q_full, 0, wc) && (cnt == 0 || mbar_wait(&k_full[0], 0, wc));
       if (ok && cnt > 0) {
         tc_fence_after();
         for (int i = 0; i < NH; ++i) issue_s(i, 0);
+        umma_commit(&k_empty[0]);
       }
       for (int n = 1; ok && n < cnt; ++n) {
         const int s = n % C::NS;
-        if (!mbar_wait(&kv_full[s], (n / C::NS) & 1, wc)) { ok = false; break; }
+        // V(n-1) for the P V MMAs below (loaded behind K(n-1)), then K(n) for the S MMAs
+        if (!mbar_wait(&v_full[(n - 1) % C::NS], ((n - 1) / C::NS) & 1, wc) ||
+            !mbar_wait(&k_full[s], (n / C::NS) & 1, wc)) { ok = false; break; }
         tc_fence_after();
         for (int i = 0; ok && i < NH; ++i) {
           if (!issue_pv(i, n - 1)) { ok = false; break; }
-          if (i == NH - 1) umma_commit(&kv_empty[(n - 1) % C::NS]);
+          if (i == NH - 1) umma_commit(&v_empty[(n - 1) % C::NS]);
           issue_s(i, s);                       // overwrites S_i / P_i: ordered after PV_i(n-1)
         }
+        if (ok) umma_commit(&k_empty[s]);
       }
+      if (ok && cnt > 0) ok = mbar_wait(&v_full[(cnt - 1) % C::NS], ((cnt - 1) / C::NS) & 1, wc);
       if (ok && cnt > 0) {
         for (int i = 0; ok && i < NH; ++i) {
           if (!issue_pv(i, cnt - 1)) { ok = false; break; }
           umma_commit(&o_done[i]);
         }
-        umma_commit(&kv_empty[(cnt - 1) % C::NS]);
+        umma_commit(&v_empty[(cnt - 1) % C::NS]);
       }
       umma_commit(drain);                      // completes once every MMA above is done
       mbar_wait_drain(drain, 0, p.wait_ns);
@@ -300,7 +325,9 @@ __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
         for (int c = 0; c < TILE; ++c)
           if (!((vm[c >> 5] >> (c & 31)) & 1u)) sv[c] = ninf;
       } else if (cls == 1) {                   // partial tile: tree mask in registers
-        if (!mbar_wait_warp(&kv_full[s], (n / C::NS) & 1, wc)) { ok = false; break; }
+        // the key tile's mask data arrive with its V tile; that stage is refilled only after
+        // the last P V of this tile, which waits for this warpgroup's P
+        if (!mbar_wait_warp(&v_full[s], (n / C::NS) & 1, wc)) { ok = false; break; }
         const int nr = p.tile_nruns[kt];
         const int jrel = qi - kt * TILE;       // key c is causal-visible iff c <= jrel
         uint32_t vm[4] = {0u, 0u, 0u, 0u};     // bit c: key c visible to this row
