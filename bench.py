@@ -708,6 +708,8 @@ def main():
     ap.add_argument("--shard", default="trees", choices=["trees", "heads"],
                     help="multi-rank split: 'trees' = one tree per rank (weak scaling); 'heads' = one tree "
                          "split by kv-head groups, plan replicated, no exchange (strong scaling)")
+    ap.add_argument("--bwd-split", type=int, default=0, choices=[0, 1, 2, 4],
+                    help="CTAs per key-tile column in the backward (0: the library's automatic choice)")
     ap.add_argument("--partition", action="store_true",
                     help="run the tree as gateway partitions (parent + children of the largest cut)")
     args = ap.parse_args()
@@ -724,6 +726,9 @@ def main():
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local)
+    if args.bwd_split:
+        import tree_masked_attention_plan_gb300 as tam
+        tam.tree_set_bwd_split(args.bwd_split)
     if args.ce:
         if world > 1:
             raise SystemExit("--ce runs on one GPU")

@@ -110,6 +110,8 @@ def _lib():
                                    _vp, _vp, _vp]),
         "tree_diag_gemm": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp]),
         "tree_set_wait_limit_ns": (_i32, [_i64]),
+        "tree_set_bwd_split": (_i32, [_i32]),
+        "tree_set_fwd_split": (_i32, [_i32]),
         "tree_set_timing_events": (_i32, [ctypes.POINTER(_vp), _i32]),
         "tree_selftest_timeout": (_i32, [_vp, _i64, _vp]),
         "tree_strerror": (ctypes.c_char_p, [_i32]),
@@ -318,6 +320,16 @@ def tree_set_timing_events(events):
     _check(_lib().tree_set_timing_events(arr, len(events)), "tree_set_timing_events")
 
 
+def tree_set_bwd_split(split: int = 0):
+    """CTAs per key-tile column in the backward: 0 automatic (default), or 1, 2, 4 forced."""
+    _check(_lib().tree_set_bwd_split(int(split)), "tree_set_bwd_split")
+
+
+def tree_set_fwd_split(split: int = 0):
+    """CTAs per query-tile row in the forward (split-KV): 0 automatic (default), or 1, 2, 4."""
+    _check(_lib().tree_set_fwd_split(int(split)), "tree_set_fwd_split")
+
+
 def tree_set_wait_limit_ns(ns: int):
     _check(_lib().tree_set_wait_limit_ns(int(ns)), "tree_set_wait_limit_ns")
 
@@ -339,7 +351,7 @@ def check_status(status, where="device"):
 
 
 __all__ = ["TreeError", "TreePlan", "tree_plan_query", "tree_plan_nodes", "tree_plan", "tree_rope_fwd", "tree_apply_weights",
-           "tree_attn_fwd", "tree_attn_bwd_workspace", "tree_attn_bwd", "tree_set_wait_limit_ns",
+           "tree_attn_fwd", "tree_attn_bwd_workspace", "tree_attn_bwd", "tree_set_wait_limit_ns", "tree_set_bwd_split", "tree_set_fwd_split",
            "tree_selftest_timeout", "tree_set_timing_events", "new_status", "check_status", "LIB_PATH", "TILE"]
 
 

@@ -49,11 +49,18 @@ struct BwdCfg {
   static constexpr int LIST_OFF = STG_OFF + NSTG * STG_BYTES;  // int32 query tiles of the column
   static constexpr int LCLS_OFF = LIST_OFF + kMaxList * 4;     // uint8 their tile classes
   static constexpr int BAR_OFF = LCLS_OFF + kMaxList;
-  static constexpr int NBAR = 15;
+  static constexpr int NBAR = 17;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int SMEM = MISC_OFF + 16;
   static constexpr int SMEM_ALLOC = SMEM + 1024;
   static_assert(SMEM_ALLOC <= 232448, "dynamic shared memory above the 227 KB a CTA may use");
+  // split columns: a CTA of rank > 0 leaves its fp32 dV, dK partial here after its main loop
+  // ([2][TILE][PART_ROW], rows padded by 16 bytes), over the K / V / Q / dO buffers, which are
+  // free by then; the dQ staging ring (still draining) lies beyond it
+  static constexpr int PART_ROW = HD + 4;
+  static constexpr int PART_OFF = 0;
+  static constexpr int PART_BYTES = 2 * TILE * PART_ROW * 4;
+  static_assert(PART_OFF + PART_BYTES <= STG_OFF, "partial-sum area must not overlap the dQ staging ring");
   // 16 warps = 4 warpgroups: [producer, MMA, 2 idle] [4 dQ drain] [4 + 4 elementwise]
   static constexpr int THREADS = 512;
   static constexpr int LAUNCH_REGS = 128;                      // 512 x 128 = the whole register file
@@ -90,6 +97,7 @@ struct BwdParams {
   int N, T, Npad, Hq, Hkv, grp;
   float scale, scale_log2, rope_theta;
   int gw_len, gw_tiles;      // gateway prefix (0 = none): its key tiles get CTAs of their own
+  int split;                 // CTAs per column (a cluster): CTA s takes steps s, s + split, ...
   float* dk_gw;              // [gw_len][Hkv][HD] fp32, accumulated (+=); rotated back at pos = row
   float* dv_gw;
   uint64_t wait_ns;
@@ -174,8 +182,12 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
   int32_t* list_s = reinterpret_cast<int32_t*>(sm + C::LIST_OFF);
   uint8_t* lcls_s = sm + C::LCLS_OFF;
 
+  uint64_t* peer_ready = bars + 15;            // rank 0: the other ranks' partials are in place
+  uint64_t* peer_done = bars + 16;             // rank > 0: rank 0 has read this CTA's partial
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int u = blockIdx.x;
+  // clusters of p.split CTAs share one column: rank s takes its steps s, s + split, ...
+  const int srank = p.split > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int u = blockIdx.x / p.split;
   // CTAs [0, gw_tiles Hkv): gateway key tiles, seen by every query tile of the partition
   // (they also have the longest columns, so they start first); then the own key tiles.
   const int ngw = p.gw_tiles * p.Hkv;
@@ -185,7 +197,9 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
   const int cp0 = gwc ? 0 : p.col_ptr[kt];
   const int ccnt = gwc ? p.T : p.col_ptr[kt + 1] - cp0;
   const int gw_cls = (gwc && kt == p.gw_tiles - 1 && (p.gw_len % TILE) != 0) ? 1 : 2;
-  const int total = ccnt * p.grp;               // steps: query tile (outer, descending) x q head (inner)
+  const int total_all = ccnt * p.grp;           // steps: query tile (outer, descending) x q head (inner)
+  const int eff = p.split;                      // CTAs the column's steps are dealt to
+  const int total = total_all > srank ? (total_all - srank + eff - 1) / eff : 0;   // this CTA's steps
 
   // the column's query tiles and their classes, staged once
   for (int i = threadIdx.x; i < ccnt && i < kMaxList; i += blockDim.x) {
@@ -197,8 +211,9 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
   // with the group's q heads innermost, so CTAs running at the same time (whatever their key
   // tile) reach the same (query tile, head) pairs together and their dQ lines stay in L2.
   auto step_tile = [&](int n, int& h, int& qt, int& cls) {
-    const int i = ccnt - 1 - n / p.grp;
-    h = kvh * p.grp + n % p.grp;
+    const int gn = srank + n * eff;             // the step's index in the whole column
+    const int i = ccnt - 1 - gn / p.grp;
+    h = kvh * p.grp + gn % p.grp;
     if (i < kMaxList) { qt = list_s[i]; cls = lcls_s[i]; }
     else if (gwc) { qt = i; cls = gw_cls; }
     else { qt = p.col_idx[cp0 + i]; cls = p.tile_class[(size_t)qt * p.T + kt]; }
@@ -217,8 +232,14 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
     mbar_init(dq_free, 4);                      // one arrival per drain warp
     mbar_init(dkdv_done, 1);
     mbar_init(drain, 1);
+    mbar_init(peer_ready, eff > 1 ? eff - 1 : 1);
+    mbar_init(peer_done, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (p.split > 1) {
+    __syncthreads();
+    cluster_sync_all();                         // every CTA's barriers initialised before remote arrivals
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -545,120 +566,188 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
         if (lane == 0) mbar_arrive(ds_ready);
       }
     }
-    if (ok && gwc && mbar_wait_warp(dkdv_done, 0, wc)) {
-      tc_fence_after();
-      // gateway row j: dV and (rotated back at position j, the row's index on the path from the
-      // root) dK added in fp32 to the caller's accumulators, which sum over child partitions
-      const bool live = j < p.gw_len;
-      float* dvg = p.dv_gw + ((size_t)j * p.Hkv + kvh) * HD;
+    // -------------------------------------------------------------- epilogue: dV, dK rows
+    // With split columns the cluster's ranks > 0 leave their fp32 partials in shared memory and
+    // rank 0 adds them, in rank order, to its own before the write-out: the same sum whatever
+    // the timing, and nothing accumulated in global memory.
+    const bool have = ok && mbar_wait_warp(dkdv_done, 0, wc);
+    if (have) tc_fence_after();
+    const uint32_t part_s = smem_u32(sm + C::PART_OFF);
+    auto part_at = [&](int which, int col) -> uint32_t {   // which: 0 dV, 1 dK; this thread's row r
+      return part_s + static_cast<uint32_t>(((which * TILE + r) * C::PART_ROW + col) * 4);
+    };
+    if (eff > 1 && srank > 0) {
+      if (have) {
+        // a rank with no steps of the column (a short column) never wrote its accumulators:
+        // its partial is zero
+        const uint32_t keep = total > 0 ? 0xffffffffu : 0u;
 #pragma unroll 1
-      for (int jc = 0; jc < HD / 64; ++jc) {
-        const int c0 = (HD / 2) * g + 32 * jc;
-        uint32_t a[32];
-        tmem_load32(tmem + lane_off + C::DV_COL + c0, a);
-        if (live) {
-          float4* d4 = reinterpret_cast<float4*>(dvg + c0);
+        for (int jc = 0; jc < HD / 64; ++jc) {
+          const int c0 = (HD / 2) * g + 32 * jc;
+          uint32_t a[32];
+          tmem_load32(tmem + lane_off + C::DV_COL + c0, a);
 #pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            float4 t = d4[v];
-            t.x += __uint_as_float(a[4 * v]);
-            t.y += __uint_as_float(a[4 * v + 1]);
-            t.z += __uint_as_float(a[4 * v + 2]);
-            t.w += __uint_as_float(a[4 * v + 3]);
-            d4[v] = t;
+          for (int c = 0; c < 32; ++c) a[c] &= keep;
+#pragma unroll
+          for (int v = 0; v < 8; ++v) st_shared_v4(part_at(0, c0 + 4 * v), a[4 * v], a[4 * v + 1], a[4 * v + 2], a[4 * v + 3]);
+        }
+#pragma unroll 1
+        for (int jc = 0; jc < HD / 64; ++jc) {
+          const int c0 = (HD / 4) * g + 16 * jc;
+          uint32_t a[16], b[16];
+          tmem_load16(tmem + lane_off + C::DK_COL + c0, a);
+          tmem_load16(tmem + lane_off + C::DK_COL + HD / 2 + c0, b);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            a[c] &= keep;
+            b[c] &= keep;
+          }
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            st_shared_v4(part_at(1, c0 + 4 * v), a[4 * v], a[4 * v + 1], a[4 * v + 2], a[4 * v + 3]);
+            st_shared_v4(part_at(1, HD / 2 + c0 + 4 * v), b[4 * v], b[4 * v + 1], b[4 * v + 2], b[4 * v + 3]);
           }
         }
       }
-      float* dkg = p.dk_gw + ((size_t)j * p.Hkv + kvh) * HD;
-      const float posf = static_cast<float>(j);
+      named_bar_sync(2, 256);                     // every elementwise thread's rows are in place
+      if (threadIdx.x == 256) mbar_arrive_remote(mapa_shared(smem_u32(peer_ready), 0));
+      (void)mbar_wait_cluster(peer_done, 0, wc);  // rank 0 reads this area until it arrives here
+    } else {
+      int nsum = 1;                               // ranks summed: this one, then 1 .. eff-1
+      if (eff > 1) nsum = __all_sync(0xffffffffu, mbar_wait_cluster(peer_ready, 0, wc)) ? eff : 1;
+      if (have && gwc) {
+        // gateway row j: dV and (rotated back at position j, the row's index on the path from
+        // the root) dK added in fp32 to the caller's accumulators, which sum over child partitions
+        const bool live = j < p.gw_len;
+        float* dvg = p.dv_gw + ((size_t)j * p.Hkv + kvh) * HD;
 #pragma unroll 1
-      for (int jc = 0; jc < HD / 64; ++jc) {
-        const int c0 = (HD / 4) * g + 16 * jc;
-        uint32_t a[16], b[16];
-        tmem_load16(tmem + lane_off + C::DK_COL + c0, a);
-        tmem_load16(tmem + lane_off + C::DK_COL + HD / 2 + c0, b);
-        if (live) {
+        for (int jc = 0; jc < HD / 64; ++jc) {
+          const int c0 = (HD / 2) * g + 32 * jc;
+          uint32_t a[32];
+          tmem_load32(tmem + lane_off + C::DV_COL + c0, a);
+          float f[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) f[c] = __uint_as_float(a[c]);
+          add_cluster_partials(f, part_at(0, c0), nsum);
+          if (live) {
+            float4* d4 = reinterpret_cast<float4*>(dvg + c0);
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              float4 t = d4[v];
+              t.x += f[4 * v];
+              t.y += f[4 * v + 1];
+              t.z += f[4 * v + 2];
+              t.w += f[4 * v + 3];
+              d4[v] = t;
+            }
+          }
+        }
+        float* dkg = p.dk_gw + ((size_t)j * p.Hkv + kvh) * HD;
+        const float posf = static_cast<float>(j);
+#pragma unroll 1
+        for (int jc = 0; jc < HD / 64; ++jc) {
+          const int c0 = (HD / 4) * g + 16 * jc;
+          uint32_t a[16], b[16];
+          tmem_load16(tmem + lane_off + C::DK_COL + c0, a);
+          tmem_load16(tmem + lane_off + C::DK_COL + HD / 2 + c0, b);
           float lo[16], hi[16];
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
-            const float g1 = __uint_as_float(a[c]), g2 = __uint_as_float(b[c]);
-            lo[c] = g1;
-            hi[c] = g2;
+            lo[c] = __uint_as_float(a[c]);
+            hi[c] = __uint_as_float(b[c]);
+          }
+          add_cluster_partials(lo, part_at(1, c0), nsum);
+          add_cluster_partials(hi, part_at(1, HD / 2 + c0), nsum);
+          if (live) {
             if (p.rope_theta > 0.f) {
+#pragma unroll
+              for (int c = 0; c < 16; ++c) {
+                float sv, cv;
+                sincosf(posf * rope_inv_freq(c0 + c, HD, p.rope_theta), &sv, &cv);
+                const float g1 = lo[c], g2 = hi[c];
+                lo[c] = g1 * cv + g2 * sv;
+                hi[c] = g2 * cv - g1 * sv;
+              }
+            }
+            // 16 consecutive fp32 of each half row: four 16-byte read-add-writes per half
+            float4* d4 = reinterpret_cast<float4*>(dkg + c0);
+            float4* e4 = reinterpret_cast<float4*>(dkg + HD / 2 + c0);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              float4 t = d4[v], w = e4[v];
+              t.x += lo[4 * v]; t.y += lo[4 * v + 1]; t.z += lo[4 * v + 2]; t.w += lo[4 * v + 3];
+              w.x += hi[4 * v]; w.y += hi[4 * v + 1]; w.z += hi[4 * v + 2]; w.w += hi[4 * v + 3];
+              d4[v] = t;
+              e4[v] = w;
+            }
+          }
+        }
+      }
+      if (have && !gwc) {
+        // dV row j, columns [HD/2 g, HD/2 (g+1))
+        __nv_bfloat16* dvrow = p.dv + ((size_t)j * p.Hkv + kvh) * HD;
+#pragma unroll 1
+        for (int jc = 0; jc < HD / 64; ++jc) {
+          const int c0 = (HD / 2) * g + 32 * jc;
+          uint32_t a[32];
+          tmem_load32(tmem + lane_off + C::DV_COL + c0, a);
+          float f[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) f[c] = __uint_as_float(a[c]);
+          add_cluster_partials(f, part_at(0, c0), nsum);
+          if (j < p.N) {
+            uint4* d4 = reinterpret_cast<uint4*>(dvrow + c0);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              d4[v] = make_uint4(pack_bf16(f[8 * v + 0], f[8 * v + 1]), pack_bf16(f[8 * v + 2], f[8 * v + 3]),
+                                 pack_bf16(f[8 * v + 4], f[8 * v + 5]), pack_bf16(f[8 * v + 6], f[8 * v + 7]));
+          }
+        }
+        // dK row j with the inverse RoPE rotation: group g takes the pairs (c, c + HD/2),
+        // c in [HD/4 g, HD/4 (g+1))
+        __nv_bfloat16* dkrow = p.dk + ((size_t)j * p.Hkv + kvh) * HD;
+        const float posf = (j < p.N) ? static_cast<float>(p.pos[j]) : 0.f;
+#pragma unroll 1
+        for (int jc = 0; jc < HD / 64; ++jc) {
+          const int c0 = (HD / 4) * g + 16 * jc;
+          uint32_t a[16], b[16];
+          tmem_load16(tmem + lane_off + C::DK_COL + c0, a);
+          tmem_load16(tmem + lane_off + C::DK_COL + HD / 2 + c0, b);
+          float lo[16], hi[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            lo[c] = __uint_as_float(a[c]);
+            hi[c] = __uint_as_float(b[c]);
+          }
+          add_cluster_partials(lo, part_at(1, c0), nsum);
+          add_cluster_partials(hi, part_at(1, HD / 2 + c0), nsum);
+          if (p.rope_theta > 0.f) {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
               float sv, cv;
               sincosf(posf * rope_inv_freq(c0 + c, HD, p.rope_theta), &sv, &cv);
+              const float g1 = lo[c], g2 = hi[c];
               lo[c] = g1 * cv + g2 * sv;
               hi[c] = g2 * cv - g1 * sv;
             }
           }
-          // 16 consecutive fp32 of each half row: four 16-byte read-add-writes per half
-          float4* d4 = reinterpret_cast<float4*>(dkg + c0);
-          float4* e4 = reinterpret_cast<float4*>(dkg + HD / 2 + c0);
+          if (j < p.N) {
+            uint4* d4 = reinterpret_cast<uint4*>(dkrow + c0);
+            uint4* e4 = reinterpret_cast<uint4*>(dkrow + HD / 2 + c0);
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            float4 t = d4[v], u = e4[v];
-            t.x += lo[4 * v]; t.y += lo[4 * v + 1]; t.z += lo[4 * v + 2]; t.w += lo[4 * v + 3];
-            u.x += hi[4 * v]; u.y += hi[4 * v + 1]; u.z += hi[4 * v + 2]; u.w += hi[4 * v + 3];
-            d4[v] = t;
-            e4[v] = u;
+            for (int v = 0; v < 2; ++v) {
+              d4[v] = make_uint4(pack_bf16(lo[8 * v], lo[8 * v + 1]), pack_bf16(lo[8 * v + 2], lo[8 * v + 3]),
+                                 pack_bf16(lo[8 * v + 4], lo[8 * v + 5]), pack_bf16(lo[8 * v + 6], lo[8 * v + 7]));
+              e4[v] = make_uint4(pack_bf16(hi[8 * v], hi[8 * v + 1]), pack_bf16(hi[8 * v + 2], hi[8 * v + 3]),
+                                 pack_bf16(hi[8 * v + 4], hi[8 * v + 5]), pack_bf16(hi[8 * v + 6], hi[8 * v + 7]));
+            }
           }
         }
       }
-    }
-    if (ok && !gwc && mbar_wait_warp(dkdv_done, 0, wc)) {
-      tc_fence_after();
-      // dV row j, columns [HD/2 g, HD/2 (g+1))
-      __nv_bfloat16* dvrow = p.dv + ((size_t)j * p.Hkv + kvh) * HD;
-#pragma unroll 1
-      for (int jc = 0; jc < HD / 64; ++jc) {
-        const int c0 = (HD / 2) * g + 32 * jc;
-        uint32_t a[32];
-        tmem_load32(tmem + lane_off + C::DV_COL + c0, a);
-        if (j < p.N) {
-          uint4* d4 = reinterpret_cast<uint4*>(dvrow + c0);
-#pragma unroll
-          for (int v = 0; v < 4; ++v)
-            d4[v] = make_uint4(pack_bf16(__uint_as_float(a[8 * v + 0]), __uint_as_float(a[8 * v + 1])),
-                               pack_bf16(__uint_as_float(a[8 * v + 2]), __uint_as_float(a[8 * v + 3])),
-                               pack_bf16(__uint_as_float(a[8 * v + 4]), __uint_as_float(a[8 * v + 5])),
-                               pack_bf16(__uint_as_float(a[8 * v + 6]), __uint_as_float(a[8 * v + 7])));
-        }
-      }
-      // dK row j with the inverse RoPE rotation: group g takes the pairs (c, c + HD/2),
-      // c in [HD/4 g, HD/4 (g+1))
-      __nv_bfloat16* dkrow = p.dk + ((size_t)j * p.Hkv + kvh) * HD;
-      const float posf = (j < p.N) ? static_cast<float>(p.pos[j]) : 0.f;
-#pragma unroll 1
-      for (int jc = 0; jc < HD / 64; ++jc) {
-        const int c0 = (HD / 4) * g + 16 * jc;
-        uint32_t a[16], b[16];
-        tmem_load16(tmem + lane_off + C::DK_COL + c0, a);
-        tmem_load16(tmem + lane_off + C::DK_COL + HD / 2 + c0, b);
-        float lo[16], hi[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float g1 = __uint_as_float(a[c]), g2 = __uint_as_float(b[c]);
-          if (p.rope_theta > 0.f) {
-            float sv, cv;
-            sincosf(posf * rope_inv_freq(c0 + c, HD, p.rope_theta), &sv, &cv);
-            lo[c] = g1 * cv + g2 * sv;
-            hi[c] = g2 * cv - g1 * sv;
-          } else {
-            lo[c] = g1;
-            hi[c] = g2;
-          }
-        }
-        if (j < p.N) {
-          uint4* d4 = reinterpret_cast<uint4*>(dkrow + c0);
-          uint4* e4 = reinterpret_cast<uint4*>(dkrow + HD / 2 + c0);
-#pragma unroll
-          for (int v = 0; v < 2; ++v) {
-            d4[v] = make_uint4(pack_bf16(lo[8 * v], lo[8 * v + 1]), pack_bf16(lo[8 * v + 2], lo[8 * v + 3]),
-                               pack_bf16(lo[8 * v + 4], lo[8 * v + 5]), pack_bf16(lo[8 * v + 6], lo[8 * v + 7]));
-            e4[v] = make_uint4(pack_bf16(hi[8 * v], hi[8 * v + 1]), pack_bf16(hi[8 * v + 2], hi[8 * v + 3]),
-                               pack_bf16(hi[8 * v + 4], hi[8 * v + 5]), pack_bf16(hi[8 * v + 6], hi[8 * v + 7]));
-          }
-        }
+      if (eff > 1) {
+        named_bar_sync(2, 256);                   // every thread has read the other ranks' areas
+        if (threadIdx.x == 256)
+          for (int q = 1; q < eff; ++q) mbar_arrive_remote(mapa_shared(smem_u32(peer_done), q));
       }
     }
   }
@@ -772,12 +861,42 @@ int launch_bwd(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k, 
         reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dO), lse, ndlt, nlse2, scale, dqacc, N, Npad,
         Hq);
   }
+  // CTAs per column: small grids split every column over a cluster (see tree_set_bwd_split)
+  const int ctas = (T + G) * Hkv;
+  int dev = 0, sms = 0;
+  rc = record_cuda(cudaGetDevice(&dev));
+  if (!rc) rc = record_cuda(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  if (rc) return rc;
+  // Clusters are used only where the grid leaves SMs idle anyway: a cluster needs all its SMs
+  // free at once, which costs throughput on a full GPU (measured: no gain at 216 CTAs on 152 SMs)
+  int split = bwd_split_override();
+  if (split == 0) {
+    split = 1;
+    while (split < 4 && (int64_t)ctas * split * 2 <= sms) split *= 2;
+  }
   BwdParams P{plan->col_ptr, plan->col_idx, plan->col_order, plan->tok_in, plan->tok_out, plan->pos,
               plan->tile_runs, plan->tile_nruns, plan->tile_class, nlse2, ndlt, dqacc, reinterpret_cast<__nv_bfloat16*>(dk),
               reinterpret_cast<__nv_bfloat16*>(dv), status, N, T, Npad, Hq, Hkv, Hq / Hkv, scale,
-              scale * 1.4426950408889634f, theta, A, G, dk_gw, dv_gw, wait_limit_ns()};
+              scale * 1.4426950408889634f, theta, A, G, split, dk_gw, dv_gw, wait_limit_ns()};
   record_timing_event(1, s);
-  k_bwd_dkdv<HD><<<(T + G) * Hkv, C::THREADS, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, tkg, tvg, P);
+  if (split == 1) {
+    k_bwd_dkdv<HD><<<ctas, C::THREADS, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, tkg, tvg, P);
+  } else {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(ctas * split);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_ALLOC;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = split;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    rc = record_cuda(cudaLaunchKernelEx(&cfg, k_bwd_dkdv<HD>, tq, tk, tv, tdo, tkg, tvg, P));
+    if (rc) return rc;
+  }
   record_timing_event(2, s);
   {
     int hpb = 1;                                  // heads per block: the largest divisor of Hq up to 8

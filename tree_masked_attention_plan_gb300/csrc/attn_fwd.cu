@@ -29,6 +29,7 @@ namespace ta {
 namespace {
 
 constexpr int kMaxList = 1024;      // row lists up to this length are staged in shared memory
+constexpr int kGwBit = 4;           // tile class flag of a gateway tile (class in the low bits)
 
 template <int HD, int NH>
 struct FwdCfg {
@@ -43,7 +44,7 @@ struct FwdCfg {
   static constexpr int LIST_OFF = RUNS_OFF + NS * TREE_MAX_RUNS * 16;   // int32 key tiles of the row
   static constexpr int LCLS_OFF = LIST_OFF + kMaxList * 4;     // uint8 their tile classes
   static constexpr int BAR_OFF = LCLS_OFF + kMaxList;
-  static constexpr int NBAR = 1 + 4 * NS + 3 * NH + 1;  // q, k and v full/empty, s/p/o per head, drain
+  static constexpr int NBAR = 1 + 4 * NS + 3 * NH + 3;  // q, k and v full/empty, s/p/o per head, drain, peers
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int SMEM = MISC_OFF + 16;
   static constexpr int SMEM_ALLOC = SMEM + 1024;      // slack for 1024-byte alignment
@@ -64,6 +65,12 @@ struct FwdCfg {
   static constexpr uint32_t V_TX = NCH * CHUNK_BYTES + 2 * TILE * 4 + TREE_MAX_RUNS * 16;   // V + mask data
   static constexpr uint32_t VG_TX = NCH * CHUNK_BYTES;                // a gateway tile: V only
   static constexpr float RESCALE_THRESHOLD = 8.f;     // log2 units
+  // split rows: a CTA of rank > 0 leaves its per-row softmax state (O row scaled by 2^-m_ref,
+  // then m_ref and l) here after its main loop, over the Q and K / V buffers, free by then
+  static constexpr int PART_ROW = HD + 4;
+  static constexpr int PART_OFF = 0;
+  static constexpr int PART_BYTES = NH * TILE * PART_ROW * 4;
+  static_assert(PART_OFF + PART_BYTES <= KIN_OFF, "partial-state area must stay below the mask data");
 };
 
 struct FwdParams {
@@ -80,6 +87,7 @@ struct FwdParams {
   int32_t* status;
   int N, T, Npad, Hq, grp, n_hgroups;
   int gw_len, gw_tiles;      // gateway prefix: keys every query sees (0 = none), its 128-key tiles
+  int split;                 // CTAs per row (a cluster): CTA s takes the row's tiles s, s + split, ...
   float scale_log2;          // softmax scale * log2(e)
   uint64_t wait_ns;
 };
@@ -116,34 +124,45 @@ __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
   uint64_t* p_full = s_full + NH;                     // [NH] P_i(n) in TMEM, O_i rescaled
   uint64_t* o_done = p_full + NH;                     // [NH] last PV_i done
   uint64_t* drain = o_done + NH;
+  uint64_t* peer_ready = drain + 1;                   // rank 0: the other ranks' row states are in place
+  uint64_t* peer_done = drain + 2;                    // rank > 0: rank 0 has read this CTA's states
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::MISC_OFF);
   int* abort_flag = reinterpret_cast<int*>(sm + C::MISC_OFF + 4);
   int32_t* kin_s = reinterpret_cast<int32_t*>(sm + C::KIN_OFF);
   int32_t* kout_s = reinterpret_cast<int32_t*>(sm + C::KOUT_OFF);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int u = blockIdx.x;
+  // clusters of p.split CTAs share one row: rank s takes the row's tiles s, s + split, ...; their
+  // softmax states are merged at the end (the associative (max, numerator, denominator) merge)
+  const int srank = p.split > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int u = blockIdx.x / p.split;
   const int qt = p.row_order[u / p.n_hgroups];
   const int h0 = (u % p.n_hgroups) * NH;              // first q head of this CTA
   const int kvh = h0 / p.grp;
   const int rp0 = p.row_ptr[qt];
   const int rcnt = p.row_ptr[qt + 1] - rp0;
   const int G = GW ? p.gw_tiles : 0;
-  const int cnt = G + rcnt;                           // gateway tiles first, then the row's own
+  const int cnt_all = G + rcnt;                       // gateway tiles first, then the row's own
+  const int cnt = cnt_all > srank ? (cnt_all - srank + p.split - 1) / p.split : 0;   // this CTA's
   int32_t* list_s = reinterpret_cast<int32_t*>(sm + C::LIST_OFF);
   uint8_t* lcls_s = sm + C::LCLS_OFF;
-  for (int i = threadIdx.x; i < rcnt && i < kMaxList; i += blockDim.x) {   // the row's key tiles, staged once
-    const int kt = p.row_idx[rp0 + i];
-    list_s[i] = kt;
-    lcls_s[i] = p.tile_class[(size_t)qt * p.T + kt];
+  // this CTA's tiles of the row (gateway tiles first), in its order, as key tile and class:
+  // global tile n of the row is gateway tile n < G (every key before gw_len visible; the last
+  // one partial when gw_len is not a multiple of 128), else the row's own tile n - G
+  auto global_tile = [&](int n, int& kt, int& cls) {
+    if (GW && n < G) { kt = n; cls = kGwBit | ((n == G - 1 && (p.gw_len % TILE) != 0) ? 1 : 2); return; }
+    kt = p.row_idx[rp0 + n - G];
+    cls = p.tile_class[(size_t)qt * p.T + kt];
+  };
+  for (int m = threadIdx.x; m < cnt && m < kMaxList; m += blockDim.x) {   // staged once
+    int kt, cls;
+    global_tile(srank + m * p.split, kt, cls);
+    list_s[m] = kt;
+    lcls_s[m] = static_cast<uint8_t>(cls);
   }
-  // step n -> key tile and class; gateway tile n < G: every key before gw_len is visible (the
-  // last one is partial when gw_len is not a multiple of 128: keys past gw_len are masked)
-  auto row_tile = [&](int n, int& kt, int& cls) {
-    if (GW && n < G) { kt = n; cls = (n == G - 1 && (p.gw_len % TILE) != 0) ? 1 : 2; return; }
-    n -= G;
-    if (n < kMaxList) { kt = list_s[n]; cls = lcls_s[n]; }
-    else { kt = p.row_idx[rp0 + n]; cls = p.tile_class[(size_t)qt * p.T + kt]; }
+  auto row_tile = [&](int m, int& kt, int& cls) {     // this CTA's tile m
+    if (m < kMaxList) { kt = list_s[m]; cls = lcls_s[m]; }
+    else global_tile(srank + m * p.split, kt, cls);
   };
 
   if (threadIdx.x == 0) {
@@ -156,6 +175,8 @@ __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
     }
     for (int i = 0; i < NH; ++i) { mbar_init(&s_full[i], 1); mbar_init(&p_full[i], 4); mbar_init(&o_done[i], 1); }
     mbar_init(drain, 1);
+    mbar_init(peer_ready, p.split > 1 ? p.split - 1 : 1);
+    mbar_init(peer_done, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -166,6 +187,7 @@ __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (p.split > 1) cluster_sync_all();                // every CTA's barriers initialised before remote arrivals
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{abort_flag, p.status, p.wait_ns};
 
@@ -177,10 +199,14 @@ __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
       if (GW) prefetch_tmap(&tmKg);
-      mbar_expect_tx(q_full, NH * C::NCH * CHUNK_BYTES);
-      for (int i = 0; i < NH; ++i)
-        for (int c = 0; c < C::NCH; ++c)
-          tma_load_3d(sm + C::Q_OFF + (i * C::NCH + c) * CHUNK_BYTES, &tmQ, q_full, c * 64, h0 + i, qt * TILE);
+      // a CTA without tiles (a split row shorter than the cluster) loads nothing: its shared
+      // memory then holds only the zero state it leaves for rank 0
+      if (cnt > 0) {
+        mbar_expect_tx(q_full, NH * C::NCH * CHUNK_BYTES);
+        for (int i = 0; i < NH; ++i)
+          for (int c = 0; c < C::NCH; ++c)
+            tma_load_3d(sm + C::Q_OFF + (i * C::NCH + c) * CHUNK_BYTES, &tmQ, q_full, c * 64, h0 + i, qt * TILE);
+      }
       // K(n) waits only for the S MMAs of tile n-2 (k_empty), not for its P V MMAs
       int issued = 0;
       for (int n = 0; n < cnt; ++n) {
@@ -190,12 +216,12 @@ __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
         if (n >= C::NS && !mbar_wait(&k_empty[s], ((n / C::NS) - 1) & 1, wc)) break;
         mbar_expect_tx(&k_full[s], C::K_TX);
         for (int c = 0; c < C::NCH; ++c)          // gateway tile rows past gw_len read as 0
-          tma_load_3d(sm + C::K_OFF + (s * C::NCH + c) * CHUNK_BYTES, (GW && n < G) ? &tmKg : &tmK, &k_full[s],
+          tma_load_3d(sm + C::K_OFF + (s * C::NCH + c) * CHUNK_BYTES, (GW && (cls & kGwBit)) ? &tmKg : &tmK, &k_full[s],
                       c * 64, kvh, kt * TILE);
         issued = n + 1;
       }
       if (*abort_flag) {                       // let copies in flight land before exit
-        mbar_wait_drain(q_full, 0, p.wait_ns);
+        if (cnt > 0) mbar_wait_drain(q_full, 0, p.wait_ns);
         for (int n = (issued > C::NS ? issued - C::NS : 0); n < issued; ++n)
           mbar_wait_drain(&k_full[n % C::NS], (n / C::NS) & 1, p.wait_ns);
       }
@@ -210,7 +236,7 @@ __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
         const int s = n % C::NS;
         int kt, cls;
         row_tile(n, kt, cls);
-        const bool gwt = GW && n < G;
+        const bool gwt = GW && (cls & kGwBit);
         if (n >= C::NS && !mbar_wait(&v_empty[s], ((n / C::NS) - 1) & 1, wc)) break;
         mbar_expect_tx(&v_full[s], gwt ? C::VG_TX : C::V_TX);
         for (int c = 0; c < C::NCH; ++c)
@@ -253,7 +279,7 @@ __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
                            (m > 0 || kk > 0) ? 1u : 0u);
         return true;
       };
-      bool ok = mbar_wait(q_full, 0, wc) && (cnt == 0 || mbar_wait(&k_full[0], 0, wc));
+      bool ok = cnt == 0 || (mbar_wait(q_full, 0, wc) && mbar_wait(&k_full[0], 0, wc));
       if (ok && cnt > 0) {
         tc_fence_after();
         for (int i = 0; i < NH; ++i) issue_s(i, 0);
@@ -317,7 +343,7 @@ __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
       tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(sv + 32));
       tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(sv + 64));
       tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(sv + 96));
-      if (GW && cls == 1 && n < G) {           // ragged last gateway tile: keys past gw_len
+      if (GW && cls == (kGwBit | 1)) {         // ragged last gateway tile: keys past gw_len
         uint32_t vm[4] = {0u, 0u, 0u, 0u};
         set_bits(vm, 0, p.gw_len - kt * TILE);
         const uint32_t ninf = __float_as_uint(-INFINITY);
@@ -416,29 +442,98 @@ __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[wg]);                 // one arrival per warp
     }
-    if (ok && cnt > 0 && mbar_wait_warp(&o_done[wg], 0, wc)) {
-      tc_fence_after();
-      const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-      __nv_bfloat16* orow = p.o + ((size_t)qi * p.Hq + h) * HD;
+    // ---------------------------------------------------------- epilogue: O, LSE of row r
+    // With split rows the cluster's ranks > 0 leave their (m_ref, l, O) here and rank 0 merges
+    // them with its own by the associative rule: m = max m_q, l = sum l_q 2^(m_q - m),
+    // O = sum O_q 2^(m_q - m); the output is O / l and LSE = m + log2 l (natural log on store).
+    const bool have = ok && cnt > 0 && mbar_wait_warp(&o_done[wg], 0, wc);
+    if (have) tc_fence_after();
+    const uint32_t part_row = smem_u32(sm + C::PART_OFF) + static_cast<uint32_t>((wg * TILE + r) * C::PART_ROW * 4);
+    if (p.split > 1 && srank > 0) {
+      const uint32_t keep = have ? 0xffffffffu : 0u;  // a rank without tiles contributes l = 0
 #pragma unroll 1
       for (int j = 0; j < HD / 32; ++j) {
         uint32_t rr[32];
         tmem_load32(o_addr + j * 32, rr);
-        if (qi < p.N) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + j * 32);
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const int c = v * 8;
-            dst[v] = make_uint4(
-                pack_bf16(__uint_as_float(rr[c + 0]) * inv_l, __uint_as_float(rr[c + 1]) * inv_l),
-                pack_bf16(__uint_as_float(rr[c + 2]) * inv_l, __uint_as_float(rr[c + 3]) * inv_l),
-                pack_bf16(__uint_as_float(rr[c + 4]) * inv_l, __uint_as_float(rr[c + 5]) * inv_l),
-                pack_bf16(__uint_as_float(rr[c + 6]) * inv_l, __uint_as_float(rr[c + 7]) * inv_l));
+        for (int v = 0; v < 8; ++v)
+          st_shared_v4(part_row + (32 * j + 4 * v) * 4, rr[4 * v] & keep, rr[4 * v + 1] & keep, rr[4 * v + 2] & keep,
+                       rr[4 * v + 3] & keep);
+      }
+      st_shared_v4(part_row + HD * 4, __float_as_uint(m_ref) & keep, __float_as_uint(l_run) & keep, 0u, 0u);
+      named_bar_sync(2, NH * 128);                     // every softmax thread's row is in place
+      if (threadIdx.x == 128) mbar_arrive_remote(mapa_shared(smem_u32(peer_ready), 0));
+      (void)mbar_wait_cluster(peer_done, 0, wc);       // rank 0 reads this area until it arrives here
+    } else {
+      int nsum = 1;                                    // ranks merged: this one, then 1 .. split-1
+      if (p.split > 1) nsum = __all_sync(0xffffffffu, mbar_wait_cluster(peer_ready, 0, wc)) ? p.split : 1;
+      float wq[4] = {1.f, 0.f, 0.f, 0.f};              // each rank's weight 2^(m_q - m)
+      float L = have ? l_run : 0.f, M = m_ref;
+      if (nsum > 1) {
+        float mq[4], lq[4];
+        mq[0] = m_ref;
+        lq[0] = have ? l_run : 0.f;
+#pragma unroll
+        for (int q = 1; q < 4; ++q) {
+          mq[q] = 0.f;
+          lq[q] = 0.f;
+          if (q < nsum) {
+            const float4 t = ld_dsmem_f4(mapa_shared(part_row + HD * 4, static_cast<uint32_t>(q)));
+            mq[q] = t.x;
+            lq[q] = t.y;
           }
         }
+        M = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (lq[q] > 0.f) M = fmaxf(M, mq[q]);
+        L = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          wq[q] = lq[q] > 0.f ? ex2_approx(mq[q] - M) : 0.f;
+          L += lq[q] * wq[q];
+        }
       }
-      p.lse[(size_t)h * p.Npad + qi] =
-          (qi < p.N && l_run > 0.f) ? (m_ref + log2f(l_run)) * 0.69314718055994531f : 0.f;
+      if (have || nsum > 1) {
+        const float inv_l = L > 0.f ? 1.f / L : 0.f;
+        __nv_bfloat16* orow = p.o + ((size_t)qi * p.Hq + h) * HD;
+#pragma unroll 1
+        for (int j = 0; j < HD / 32; ++j) {
+          uint32_t rr[32];
+          tmem_load32(o_addr + j * 32, rr);
+          float of[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) of[c] = have ? __uint_as_float(rr[c]) * wq[0] : 0.f;
+#pragma unroll
+          for (int q = 1; q < 4; ++q) {
+            if (q < nsum && wq[q] != 0.f) {
+#pragma unroll
+              for (int v = 0; v < 8; ++v) {
+                const float4 t = ld_dsmem_f4(mapa_shared(part_row + (32 * j + 4 * v) * 4, static_cast<uint32_t>(q)));
+                of[4 * v] += t.x * wq[q];
+                of[4 * v + 1] += t.y * wq[q];
+                of[4 * v + 2] += t.z * wq[q];
+                of[4 * v + 3] += t.w * wq[q];
+              }
+            }
+          }
+          if (qi < p.N) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + j * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const int c = v * 8;
+              dst[v] = make_uint4(pack_bf16(of[c + 0] * inv_l, of[c + 1] * inv_l), pack_bf16(of[c + 2] * inv_l, of[c + 3] * inv_l),
+                                  pack_bf16(of[c + 4] * inv_l, of[c + 5] * inv_l), pack_bf16(of[c + 6] * inv_l, of[c + 7] * inv_l));
+            }
+          }
+        }
+        p.lse[(size_t)h * p.Npad + qi] = (qi < p.N && L > 0.f) ? (M + log2f(L)) * 0.69314718055994531f : 0.f;
+      }
+      if (p.split > 1) {
+        named_bar_sync(2, NH * 128);                   // every thread has read the other ranks' areas
+        if (threadIdx.x == 128)
+          for (int q = 1; q < p.split; ++q) mbar_arrive_remote(mapa_shared(smem_u32(peer_done), q));
+      }
     }
   }
   // ---------------------------------------------------------------- teardown
@@ -460,10 +555,22 @@ int launch_fwd(const tree_plan_t* plan, const CUtensorMap& tq, const CUtensorMap
   int rc = record_cuda(
       cudaFuncSetAttribute(k_attn_fwd<HD, NH, GW>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC));
   if (rc) return rc;
+  // CTAs per row: split only where the grid leaves SMs idle anyway (a cluster needs all its SMs
+  // free at once); rows then go to clusters whose states merge at the end
+  const int ctas = T * (Hq / NH);
+  int split = fwd_split_override();
+  if (split == 0) {
+    int dev = 0, sms = 0;
+    rc = record_cuda(cudaGetDevice(&dev));
+    if (!rc) rc = record_cuda(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    if (rc) return rc;
+    split = 1;
+    while (split < 4 && (int64_t)ctas * split * 2 <= sms) split *= 2;
+  }
   FwdParams P{plan->row_ptr, plan->row_idx, plan->row_order, plan->tok_in, plan->tok_out, plan->tile_runs,
               plan->tile_nruns, plan->tile_class,
               reinterpret_cast<__nv_bfloat16*>(o), lse, status, N, T, T * TILE, Hq, Hq / Hkv, Hq / NH,
-              gw_len, (gw_len + TILE - 1) / TILE, scale * 1.4426950408889634f, wait_limit_ns()};
+              gw_len, (gw_len + TILE - 1) / TILE, split, scale * 1.4426950408889634f, wait_limit_ns()};
   if constexpr (NH == 2) {
     // setmaxnreg.inc waits for registers the other warpgroups released: the re-balancing only
     // adds up if the kernel launches with exactly LAUNCH_REGS per thread.
@@ -475,8 +582,23 @@ int launch_fwd(const tree_plan_t* plan, const CUtensorMap& tq, const CUtensorMap
       return TREE_ERR_CUDA;
     }
   }
-  k_attn_fwd<HD, NH, GW><<<T * (Hq / NH), C::THREADS, C::SMEM_ALLOC, s>>>(tq, tk, tv, tkg, tvg, P);
-  return record_cuda(cudaGetLastError());
+  if (split == 1) {
+    k_attn_fwd<HD, NH, GW><<<ctas, C::THREADS, C::SMEM_ALLOC, s>>>(tq, tk, tv, tkg, tvg, P);
+    return record_cuda(cudaGetLastError());
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(ctas * split);
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_ALLOC;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = split;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return record_cuda(cudaLaunchKernelEx(&cfg, k_attn_fwd<HD, NH, GW>, tq, tk, tv, tkg, tvg, P));
 }
 
 }  // namespace

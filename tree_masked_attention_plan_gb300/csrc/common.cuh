@@ -127,6 +127,84 @@ DEVI bool mbar_wait_warp(uint64_t* bar, uint32_t parity, const WaitCtl& wc) {
 }
 
 // ------------------------------------------------------------------------------------------
+// thread-block clusters (distributed shared memory)
+DEVI uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// address of the same shared-memory location in CTA `rank` of the cluster
+DEVI uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+// every thread of every CTA of the cluster (a hardware barrier, like __syncthreads)
+DEVI void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// arrive once on an mbarrier of another CTA of the cluster; the calling thread's earlier
+// writes (and those ordered before them) are released at cluster scope
+DEVI void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+DEVI bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+DEVI void st_shared_v4(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+DEVI float4 ld_dsmem_f4(uint32_t cluster_addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(cluster_addr)
+               : "memory");
+  return v;
+}
+
+// The same bounded wait with cluster-scope acquire: for barriers that other CTAs of the
+// cluster arrive on (their released writes are visible after it returns true).
+DEVI bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, const WaitCtl& wc) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 15u) == 0) {
+      if (*wc.abort_flag) return false;
+      if (global_timer_ns() - t0 > wc.limit_ns) {
+        *wc.abort_flag = 1;
+        if (wc.status) atomicExch(wc.status, TREE_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// v[e] += the CNT fp32 values at shared offset `saddr` of cluster ranks 1 .. nsum-1, in rank order
+template <int CNT>
+DEVI void add_cluster_partials(float (&v)[CNT], uint32_t saddr, int nsum) {
+  for (int q = 1; q < nsum; ++q) {
+#pragma unroll
+    for (int e = 0; e < CNT; e += 4) {
+      const float4 t = ld_dsmem_f4(mapa_shared(saddr + 4 * e, static_cast<uint32_t>(q)));
+      v[e] += t.x;
+      v[e + 1] += t.y;
+      v[e + 2] += t.z;
+      v[e + 3] += t.w;
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------
 // TMA
 DEVI void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
@@ -386,6 +464,8 @@ int record_cuda(cudaError_t e);                      // TREE_OK or TREE_ERR_CUDA
 int make_tmap_bf16_3d(CUtensorMap* m, const void* base, int d, int heads, int rows);
 int make_tmap_f32_2d(CUtensorMap* m, const void* base, int inner, int rows, int box_inner, int box_rows);
 uint64_t wait_limit_ns();
+int bwd_split_override();                            // 0: automatic
+int fwd_split_override();                            // 0: automatic
 int plan_ok(const tree_plan_t* p);
 void record_timing_event(int i, cudaStream_t s);     // no-op unless events are registered
 }  // namespace ta

@@ -13,6 +13,8 @@ namespace ta {
 
 static thread_local char g_last_err[256] = "";
 static std::atomic<int64_t> g_wait_limit_ns{2000000000LL};
+static std::atomic<int> g_bwd_split{0};         // 0: chosen per launch from the grid size
+static std::atomic<int> g_fwd_split{0};
 
 int record_cuda(cudaError_t e) {
   if (e == cudaSuccess) return TREE_OK;
@@ -152,6 +154,8 @@ void record_timing_event(int i, cudaStream_t s) {
 }
 
 uint64_t wait_limit_ns() { return static_cast<uint64_t>(g_wait_limit_ns.load()); }
+int bwd_split_override() { return g_bwd_split.load(); }
+int fwd_split_override() { return g_fwd_split.load(); }
 
 int plan_ok(const tree_plan_t* p) {
   if (!p || !p->tok_in || !p->row_ptr || !p->row_idx || !p->col_ptr || !p->col_idx || !p->tile_class ||
@@ -187,6 +191,18 @@ int tree_set_timing_events(void* const* events, int n) {
   if (n < 0 || n > 4 || (n > 0 && !events)) return TREE_ERR_ARG;
   for (int i = 0; i < 4; ++i) g_events[i] = i < n ? static_cast<cudaEvent_t>(events[i]) : nullptr;
   g_n_events = n;
+  return TREE_OK;
+}
+
+int tree_set_fwd_split(int split) {
+  if (split != 0 && split != 1 && split != 2 && split != 4) return TREE_ERR_ARG;
+  g_fwd_split.store(split);
+  return TREE_OK;
+}
+
+int tree_set_bwd_split(int split) {
+  if (split != 0 && split != 1 && split != 2 && split != 4) return TREE_ERR_ARG;
+  g_bwd_split.store(split);
   return TREE_OK;
 }
 
