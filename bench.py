@@ -710,6 +710,8 @@ def main():
                          "split by kv-head groups, plan replicated, no exchange (strong scaling)")
     ap.add_argument("--bwd-split", type=int, default=0, choices=[0, 1, 2, 4],
                     help="CTAs per key-tile column in the backward (0: the library's automatic choice)")
+    ap.add_argument("--fwd-split", type=int, default=0, choices=[0, 1, 2, 4],
+                    help="CTAs per query-tile row in the forward, split-KV (0: automatic)")
     ap.add_argument("--partition", action="store_true",
                     help="run the tree as gateway partitions (parent + children of the largest cut)")
     args = ap.parse_args()
@@ -726,9 +728,10 @@ def main():
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local)
-    if args.bwd_split:
+    if args.bwd_split or args.fwd_split:
         import tree_masked_attention_plan_gb300 as tam
         tam.tree_set_bwd_split(args.bwd_split)
+        tam.tree_set_fwd_split(args.fwd_split)
     if args.ce:
         if world > 1:
             raise SystemExit("--ce runs on one GPU")

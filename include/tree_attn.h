@@ -363,10 +363,11 @@ int tree_diag_gemm(const tree_bf16* A, const tree_bf16* B, int M, int N, int K, 
  * column runs as a thread-block cluster: CTA r of the cluster takes the column's steps
  * r, r + s, r + 2s, ... (s = the split) and the cluster sums its fp32 dK / dV partials through
  * distributed shared memory, in rank order, before the single write-out (deterministic).
- * Automatic: the largest of 1, 2, 4 for which the grid (key tiles x kv heads x split) fills at
- * most half the SMs, i.e. only trees too small to occupy the GPU are split (a cluster needs all
- * its SMs free at once, which costs throughput on a busy GPU).  Process-wide; for tests and
- * measurements.  Other values -> TREE_ERR_ARG. */
+ * Automatic: the largest of 1, 2, 4 for which the split grid (key tiles x kv heads x split)
+ * still fits one wave of SMs, i.e. only trees too small to occupy the GPU are split (a cluster
+ * needs all its SMs free at once, which costs throughput on a busy GPU: measured no gain for
+ * 216 columns on 152 SMs).  Process-wide; for tests and measurements.  Other values ->
+ * TREE_ERR_ARG. */
 int tree_set_bwd_split(int split);
 
 /* CTAs per query-tile row in the forward (1, 2 or 4; 0 = automatic, the default): split-KV.  A
@@ -374,9 +375,10 @@ int tree_set_bwd_split(int split);
  * r, r + s, r + 2s, ... (gateway tiles included) with its own online-softmax state (m, l, O),
  * and rank 0 merges the states by the Tree Attention page's associative rule
  * (m = max m_r, l = sum l_r 2^(m_r - m), O = sum O_r 2^(m_r - m)) read through distributed
- * shared memory before writing O / l and the LSE.  Automatic: as for the backward, the largest
- * of 1, 2, 4 for which the grid (query tiles x q-head pairs x split) fills at most half the SMs
- * (e.g. a small partition below a long gateway).  Process-wide.  Other values -> TREE_ERR_ARG. */
+ * shared memory before writing O / l and the LSE.  Automatic: the largest of 1, 2, 4 for which
+ * the grid (query tiles x q-head pairs x split) fits one wave of SMs (e.g. a small partition
+ * below a long gateway: 256 tokens below 32768, forward 444 -> 174 us).  Process-wide.  Other
+ * values -> TREE_ERR_ARG. */
 int tree_set_fwd_split(int split);
 
 /* Device waits give up after this many nanoseconds and report TREE_ERR_TIMEOUT

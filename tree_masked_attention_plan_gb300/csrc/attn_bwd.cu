@@ -867,12 +867,13 @@ int launch_bwd(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k, 
   rc = record_cuda(cudaGetDevice(&dev));
   if (!rc) rc = record_cuda(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   if (rc) return rc;
-  // Clusters are used only where the grid leaves SMs idle anyway: a cluster needs all its SMs
-  // free at once, which costs throughput on a full GPU (measured: no gain at 216 CTAs on 152 SMs)
+  // Clusters are used only while the split grid still fits one wave of SMs: a cluster needs all
+  // its SMs free at once, which costs throughput on a full GPU (measured: no gain at 216 CTAs
+  // on 152 SMs, and a 2064-CTA gateway backward 0.51 -> 0.91 ms when forced to 2)
   int split = bwd_split_override();
   if (split == 0) {
     split = 1;
-    while (split < 4 && (int64_t)ctas * split * 2 <= sms) split *= 2;
+    while (split < 4 && (int64_t)ctas * split * 2 <= sms) split *= 2;   // the doubled grid fits one wave
   }
   BwdParams P{plan->col_ptr, plan->col_idx, plan->col_order, plan->tok_in, plan->tok_out, plan->pos,
               plan->tile_runs, plan->tile_nruns, plan->tile_class, nlse2, ndlt, dqacc, reinterpret_cast<__nv_bfloat16*>(dk),
