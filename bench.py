@@ -140,6 +140,16 @@ class ClockSampler:
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+        # nvidia-smi's start-up (driver queries) must not overlap the timed region: wait for its
+        # first sample line (at most 10 s), then a little more
+        t0 = time.time()
+        while self.proc is not None and time.time() - t0 < 10.0:
+            try:
+                if os.path.getsize(self.path) > 0:
+                    break
+            except OSError:
+                pass
+            time.sleep(0.05)
         time.sleep(0.3)
         return self
 
