@@ -79,7 +79,39 @@ def partition_tree(parent, node_len, cut: int) -> dict:
     children = [_part(parent, node_len, starts, cs, A) for cs in child_sets if node_len[cs].sum() > 0]
     where = np.empty(int(node_len.sum()), dtype=np.int64)
     where[ppart.tokens] = np.arange(len(ppart.tokens))
-    return dict(parent=ppart, children=children, gw_tokens=gw_tokens, gw_rows=where[gw_tokens], A=A)
+    return dict(parent=ppart, children=children, gw_tokens=gw_tokens, gw_rows=where[gw_tokens], A=A, cut=int(cut))
+
+
+def context_tree(part: Partition, ctx_len: int):
+    """A child partition's tree with one more root in front (node 0, holding `ctx_len` tokens):
+    the partition's nodes follow as ids 1.., their root now a child of node 0, so depth-first
+    packing puts the context tokens first and the partition's tokens after them in partition
+    order.  Layers that carry context along root paths (section 9) run on this tree:
+    * causal convolution with K taps: node 0 holds the gateway path's last min(K-1, A) tokens
+      (their rows gathered from the parent partition), its upstream gradient rows are zero, and
+      the gradient its rows receive is the child's contribution to those gateway tokens;
+    * recurrent-state routing: node 0 (ctx_len >= 1) carries the state the gateway path ends
+      with, which every node of the partition that has no token-holding ancestor inside it
+      starts from; the routing backward's gradient for node 0 goes to that gateway node."""
+    if ctx_len < 0:
+        raise ValueError("ctx_len must be >= 0")
+    parent = np.concatenate([[-1], np.where(part.parent < 0, 0, part.parent + 1)]).astype(np.int64)
+    node_len = np.concatenate([[ctx_len], part.node_len]).astype(np.int64)
+    return parent, node_len
+
+
+def gateway_state_node(P: dict, parent, node_len) -> int:
+    """Index, inside the parent partition of partition_tree's result P, of the node whose final
+    recurrent state the child partitions start from: the cut node if it holds tokens, else its
+    nearest ancestor that does (-1 if none: the children start from zeros)."""
+    parent = np.asarray(parent, dtype=np.int64)
+    node_len = np.asarray(node_len, dtype=np.int64)
+    ppart = P["parent"]
+    where = {int(v): i for i, v in enumerate(ppart.nodes)}
+    v = int(P["cut"])
+    while v >= 0 and node_len[v] == 0:
+        v = int(parent[v])
+    return where[v] if v >= 0 else -1
 
 
 def largest_cut(parent, node_len):
