@@ -36,10 +36,12 @@ struct BwdCfg {
   static constexpr int NCH = HD / 64;
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = K_OFF + NCH * CHUNK_BYTES;
-  static constexpr int Q_OFF = V_OFF + NCH * CHUNK_BYTES;     // two stages
+  // Q is loaded twice per step: once for S^T = K Q^T (freed as soon as that product is done,
+  // so the next step's copy has a whole step to arrive) and once for dK += dS^T Q
+  static constexpr int Q_OFF = V_OFF + NCH * CHUNK_BYTES;     // [Q for S][Q for dK]
   static constexpr int DO_OFF = Q_OFF + 2 * NCH * CHUNK_BYTES;
   static constexpr int DST_OFF = DO_OFF + NCH * CHUNK_BYTES;
-  // per Q stage, loaded with the Q tile: -LSE log2e, -delta scale, query dfs_in, node runs of the query tile
+  // per step, in a ring of two stages: -LSE log2e, -delta scale, query dfs_in, node runs of the query tile
   static constexpr int AUX_LSE = 0, AUX_DLT = TILE * 4, AUX_QIN = 2 * TILE * 4, AUX_RUNS = 3 * TILE * 4;
   static constexpr int AUX_BYTES = AUX_RUNS + TREE_MAX_RUNS * 16;
   static constexpr int AUX_OFF = DST_OFF + 2 * CHUNK_BYTES;    // two stages
@@ -49,7 +51,7 @@ struct BwdCfg {
   static constexpr int LIST_OFF = STG_OFF + NSTG * STG_BYTES;  // int32 query tiles of the column
   static constexpr int LCLS_OFF = LIST_OFF + kMaxList * 4;     // uint8 their tile classes
   static constexpr int BAR_OFF = LCLS_OFF + kMaxList;
-  static constexpr int NBAR = 17;
+  static constexpr int NBAR = 21;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int SMEM = MISC_OFF + 16;
   static constexpr int SMEM_ALLOC = SMEM + 1024;
@@ -74,7 +76,7 @@ struct BwdCfg {
   static constexpr uint32_t IDESC_DKV = idesc_bf16(TILE, HD, 0, 1);     // P^T (TMEM) / dS^T K-major, dO/Q MN-major
   static constexpr uint32_t IDESC_DQ = idesc_bf16(TILE, HD, 1, 1);      // dS MN-major, K MN-major
   static constexpr uint32_t KV_TX = 2 * NCH * CHUNK_BYTES;
-  static constexpr uint32_t Q_TX = NCH * CHUNK_BYTES + AUX_BYTES;
+  static constexpr uint32_t Q_TX = NCH * CHUNK_BYTES;
   static constexpr uint32_t DO_TX = NCH * CHUNK_BYTES;
 };
 
@@ -173,8 +175,8 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
   uint64_t* dq_free = bars + 6;
   uint64_t* dkdv_done = bars + 7;
   uint64_t* drain = bars + 8;
-  uint64_t* q_full = bars + 9;                  // [2] Q stages (with LSE, delta, dfs_in, runs)
-  uint64_t* q_empty = bars + 11;                // [2]
+  uint64_t* aux_full = bars + 9;                // [2] row data of a step (LSE, delta, dfs_in, runs)
+  uint64_t* aux_empty = bars + 11;              // [2] one arrival per elementwise warp after dS
   uint64_t* p_ready = bars + 13;                // P^T of both groups written
   uint64_t* ds_ready = bars + 14;               // dS^T of both groups written
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::MISC_OFF);
@@ -184,6 +186,10 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
 
   uint64_t* peer_ready = bars + 15;            // rank 0: the other ranks' partials are in place
   uint64_t* peer_done = bars + 16;             // rank > 0: rank 0 has read this CTA's partial
+  uint64_t* qs_full = bars + 17;               // Q for S^T(n) landed
+  uint64_t* qs_empty = bars + 18;              // S^T(n) done: that buffer is free
+  uint64_t* qd_full = bars + 19;               // Q for dK(n) landed
+  uint64_t* qd_empty = bars + 20;              // dK(n) done: that buffer is free
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // clusters of p.split CTAs share one column: rank s takes its steps s, s + split, ...
   const int srank = p.split > 1 ? static_cast<int>(cluster_ctarank()) : 0;
@@ -223,7 +229,11 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
     mbar_init(kv_full, 1);
     mbar_init(do_full, 1);
     mbar_init(do_empty, 1);
-    for (int i = 0; i < 2; ++i) { mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&aux_full[i], 1); mbar_init(&aux_empty[i], 8); }
+    mbar_init(qs_full, 1);
+    mbar_init(qs_empty, 1);
+    mbar_init(qd_full, 1);
+    mbar_init(qd_empty, 1);
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
     mbar_init(p_ready, 8);                      // one arrival per elementwise warp
@@ -265,13 +275,20 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
         tma_load_3d(sm + C::K_OFF + c * CHUNK_BYTES, gwc ? &tmKg : &tmK, kv_full, c * 64, kvh, kt * TILE);
         tma_load_3d(sm + C::V_OFF + c * CHUNK_BYTES, gwc ? &tmVg : &tmV, kv_full, c * 64, kvh, kt * TILE);
       }
-      auto load_q = [&](int m) {               // Q tile of step m (and its row data) into stage m % 2
+      // Q tile of step m into the buffer of the S product (which = 0) or of the dK product (1)
+      auto load_q = [&](int m, int which) {
         int h, qt, cls;
         step_tile(m, h, qt, cls);
-        uint64_t* bar = &q_full[m & 1];
+        uint64_t* bar = which ? qd_full : qs_full;
         mbar_expect_tx(bar, C::Q_TX);
         for (int c = 0; c < C::NCH; ++c)
-          tma_load_3d(sm + C::Q_OFF + ((m & 1) * C::NCH + c) * CHUNK_BYTES, &tmQ, bar, c * 64, h, qt * TILE);
+          tma_load_3d(sm + C::Q_OFF + (which * C::NCH + c) * CHUNK_BYTES, &tmQ, bar, c * 64, h, qt * TILE);
+      };
+      auto load_aux = [&](int m) {             // row data of step m into ring stage m % 2
+        int h, qt, cls;
+        step_tile(m, h, qt, cls);
+        uint64_t* bar = &aux_full[m & 1];
+        mbar_expect_tx(bar, C::AUX_BYTES);
         uint8_t* aux = sm + C::AUX_OFF + (m & 1) * C::AUX_BYTES;
         const size_t lo = (size_t)h * p.Npad + (size_t)qt * TILE;
         bulk_load(aux + C::AUX_LSE, p.nlse2 + lo, TILE * 4, bar);
@@ -279,8 +296,16 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
         bulk_load(aux + C::AUX_QIN, p.tok_in + (size_t)qt * TILE, TILE * 4, bar);
         bulk_load(aux + C::AUX_RUNS, p.tile_runs + (size_t)qt * TREE_MAX_RUNS * 4, TREE_MAX_RUNS * 16, bar);
       };
-      int q_issued = 0, do_issued = 0;
-      if (total > 0) { load_q(0); q_issued = 1; }
+      // Loads in the order their buffers free up during step n: dO(n) after dV(n-1), Q for
+      // S(n+1) after S(n), the row data of step n+1 after step n-1's dS, Q for dK(n) after dK(n-1).
+      int qs_issued = 0, qd_issued = 0, aux_issued = 0, do_issued = 0;
+      if (total > 0) {
+        load_q(0, 0);
+        load_aux(0);
+        load_q(0, 1);
+        qs_issued = qd_issued = aux_issued = 1;
+      }
+      if (total > 1) { load_aux(1); aux_issued = 2; }
       for (int n = 0; n < total; ++n) {
         int h, qt, cls;
         step_tile(n, h, qt, cls);
@@ -290,18 +315,30 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
         for (int c = 0; c < C::NCH; ++c)
           tma_load_3d(sm + C::DO_OFF + c * CHUNK_BYTES, &tmDO, do_full, c * 64, h, qt * TILE);
         do_issued = n + 1;
-        // Q of step n+1 into the other stage once dK(n-1) has read it
         if (n + 1 < total) {
-          if (n >= 1 && !mbar_wait(&q_empty[(n + 1) & 1], (((n + 1) >> 1) - 1) & 1, wc)) break;
-          load_q(n + 1);
-          q_issued = n + 2;
+          if (!mbar_wait(qs_empty, n & 1, wc)) break;
+          load_q(n + 1, 0);
+          qs_issued = n + 2;
+          // stage (n+1) % 2 held step n-1's row data until its dS phase ended
+          if (n >= 1) {
+            if (!mbar_wait(&aux_empty[(n + 1) & 1], ((n - 1) >> 1) & 1, wc)) break;
+            load_aux(n + 1);
+            aux_issued = n + 2;
+          }
+        }
+        if (n > 0) {
+          if (!mbar_wait(qd_empty, (n - 1) & 1, wc)) break;
+          load_q(n, 1);
+          qd_issued = n + 1;
         }
       }
       if (*abort_flag) {
         mbar_wait_drain_b(kv_full, 0, p.wait_ns);
         if (do_issued > 0) mbar_wait_drain_b(do_full, (do_issued - 1) & 1, p.wait_ns);
-        for (int m = (q_issued > 2 ? q_issued - 2 : 0); m < q_issued; ++m)
-          mbar_wait_drain_b(&q_full[m & 1], (m >> 1) & 1, p.wait_ns);
+        if (qs_issued > 0) mbar_wait_drain_b(qs_full, (qs_issued - 1) & 1, p.wait_ns);
+        if (qd_issued > 0) mbar_wait_drain_b(qd_full, (qd_issued - 1) & 1, p.wait_ns);
+        for (int m = (aux_issued > 2 ? aux_issued - 2 : 0); m < aux_issued; ++m)
+          mbar_wait_drain_b(&aux_full[m & 1], (m >> 1) & 1, p.wait_ns);
       }
     }
   } else if (warp == 1) {
@@ -315,22 +352,22 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
       const uint64_t v_km = sdesc_sw128(v_base, 16, 1024);
       const uint64_t do_km = sdesc_sw128(do_base, 16, 1024), do_mn = sdesc_sw128(do_base, CHUNK_BYTES, 1024);
       const uint64_t ds_km = sdesc_sw128(dst_base, 16, 1024), ds_mn = sdesc_sw128(dst_base, CHUNK_BYTES, 1024);
-      const uint64_t q_km[2] = {sdesc_sw128(q_base0, 16, 1024), sdesc_sw128(q_base1, 16, 1024)};
-      const uint64_t q_mn[2] = {sdesc_sw128(q_base0, CHUNK_BYTES, 1024), sdesc_sw128(q_base1, CHUNK_BYTES, 1024)};
+      const uint64_t qs_km = sdesc_sw128(q_base0, 16, 1024);             // Q for S, K-major
+      const uint64_t qd_mn = sdesc_sw128(q_base1, CHUNK_BYTES, 1024);    // Q for dK, MN-major
       // Software-pipelined over the steps so the tensor core runs one step's GEMMs while the
       // elementwise warps work on the other step's tile.  A holds S^T(n), then P^T(n) until dV(n);
       // B holds dP^T(n) until dS(n) is computed, then dQ(n) until the drain has read it.  Issue
       // order for step n: [dQ(n-1), dK(n-1)], dP(n), dV(n), S(n+1).
       auto issue_s = [&](int m) -> bool {       // S^T(m) = K Q(m)^T into A
-        if (!mbar_wait(&q_full[m & 1], (m >> 1) & 1, wc)) return false;
+        if (!mbar_wait(qs_full, m & 1, wc)) return false;
         tc_fence_after();
-        const uint64_t qd = q_km[m & 1];
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * CHUNK_BYTES + (kk & 3) * 32;
-          umma_bf16(tmem + C::A_COL, sdesc_adv(k_km, off), sdesc_adv(qd, off), C::IDESC_SDP, kk > 0 ? 1u : 0u);
+          umma_bf16(tmem + C::A_COL, sdesc_adv(k_km, off), sdesc_adv(qs_km, off), C::IDESC_SDP, kk > 0 ? 1u : 0u);
         }
         umma_commit(s_full);
+        umma_commit(qs_empty);                                   // Q for S free for step m+1
         return true;
       };
       // dQ(m) = dS(m) K into B first, so the drain copies it out while dK += dS(m)^T Q(m) runs
@@ -342,12 +379,13 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
           umma_bf16(tmem + C::B_COL, sdesc_adv(ds_mn, kk * 16 * 128), sdesc_adv(k_mn, kk * 16 * 128), C::IDESC_DQ,
                     kk > 0 ? 1u : 0u);
         umma_commit(dq_full);
-        const uint64_t qd = q_mn[m & 1];
+        if (!mbar_wait(qd_full, m & 1, wc)) return false;
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < TILE / 16; ++kk)
           umma_bf16(tmem + C::DK_COL, sdesc_adv(ds_km, (kk >> 2) * CHUNK_BYTES + (kk & 3) * 32),
-                    sdesc_adv(qd, kk * 16 * 128), C::IDESC_DKV, (m > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&q_empty[m & 1]);                            // this Q stage free
+                    sdesc_adv(qd_mn, kk * 16 * 128), C::IDESC_DKV, (m > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(qd_empty);                                   // Q for dK free for step m+1
         return true;
       };
       bool ok = mbar_wait(kv_full, 0, wc);
@@ -453,7 +491,7 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
     for (int n = 0; n < total; ++n) {
       int h, qt, cls;
       step_tile(n, h, qt, cls);
-      if (!mbar_wait_warp(&q_full[n & 1], (n >> 1) & 1, wc) || !mbar_wait_warp(s_full, n & 1, wc)) { ok = false; break; }
+      if (!mbar_wait_warp(&aux_full[n & 1], (n >> 1) & 1, wc) || !mbar_wait_warp(s_full, n & 1, wc)) { ok = false; break; }
       tc_fence_after();
       const uint8_t* aux = sm + C::AUX_OFF + (n & 1) * C::AUX_BYTES;
       const float* nlse_s = reinterpret_cast<const float*>(aux + C::AUX_LSE);
@@ -563,7 +601,10 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
         tc_fence_before();                        // the dP^T reads are done before dQ rewrites B
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(ds_ready);
+        if (lane == 0) {
+          mbar_arrive(ds_ready);
+          mbar_arrive(&aux_empty[n & 1]);         // this step's row data no longer read
+        }
       }
     }
     // -------------------------------------------------------------- epilogue: dV, dK rows
