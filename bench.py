@@ -275,7 +275,10 @@ def run_ours(args, rank, world, dev):
     # inputs in and its outputs out.  As a training input pipeline does, step i+1's inputs are
     # copied in and step i's outputs copied out on side streams while the next step computes
     # (two device buffers of each); the timed span runs from the first step's copy-in to the
-    # last step's copy-out, divided by the number of steps.  Inputs (671 MB) exceed L2.
+    # last step's copy-out, divided by the number of steps.  Inputs (671 MB) exceed L2.  Within a
+    # step the copies follow the data: K, V, Q come in before U (first read by the loss weights,
+    # after the forward), and O goes out as soon as the forward has written it (during the
+    # backward), dQ, dK, dV after the backward.
     o_ref, dk_ref, dv_ref = o.clone(), dk.clone(), dv.clone()
     host_in = tuple(t[x].pin_memory() for x in ("q", "k", "v", "u"))
     host_out = tuple(torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (o, dq, dk, dv))
@@ -284,41 +287,44 @@ def run_ours(args, rank, world, dev):
     ins = [(q, k, v, u), tuple(torch.empty_like(x) for x in (q, k, v, u))]
     outs = [(o, dq, dk, dv), tuple(torch.empty_like(x) for x in (o, dq, dk, dv))]
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    in_ready, comp_done, out_done = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
-
-    def step_io(p, bi, bo):
-        qq, kk, vv, uu = bi
-        oo, dqq, dkk, dvv = bo
-        tam.tree_rope_fwd(p, qq, kk, theta, qr=qr, kr=kr)
-        tam.tree_attn_fwd(p, qr, kr, vv, o=oo, lse=lse, status=status)
-        tam.tree_apply_weights(p, uu, out=dO)
-        tam.tree_attn_bwd(p, qr, kr, vv, oo, lse, dO, rope_theta=theta, workspace=ws, dq=dqq, dk=dkk, dv=dvv,
-                          status=status)
+    qkv_ready, u_ready, fwd_done, comp_done, out_done = ([torch.cuda.Event() for _ in range(2)] for _ in range(5))
 
     def copy_in(i):
         b = i % 2
         if i >= 2:
             s_in.wait_event(comp_done[b])          # step i-2 has finished reading these buffers
         with torch.cuda.stream(s_in):
-            for dst, src in zip(ins[b], host_in):
-                dst.copy_(src, non_blocking=True)
-        in_ready[b].record(s_in)
+            for j in (1, 2, 0):                    # K, V, Q: what RoPE and the forward read
+                ins[b][j].copy_(host_in[j], non_blocking=True)
+            qkv_ready[b].record(s_in)
+            ins[b][3].copy_(host_in[3], non_blocking=True)
+            u_ready[b].record(s_in)
 
     def compute(i):
         b = i % 2
-        stream.wait_event(in_ready[b])
+        qq, kk, vv, uu = ins[b]
+        oo, dqq, dkk, dvv = outs[b]
+        stream.wait_event(qkv_ready[b])
         if i >= 2:
             stream.wait_event(out_done[b])         # step i-2's outputs have left these buffers
         p = tam.tree_plan(wl.parent, wl.node_len, device=dev)
-        step_io(p, ins[b], outs[b])
+        tam.tree_rope_fwd(p, qq, kk, theta, qr=qr, kr=kr)
+        tam.tree_attn_fwd(p, qr, kr, vv, o=oo, lse=lse, status=status)
+        fwd_done[b].record(stream)
+        stream.wait_event(u_ready[b])
+        tam.tree_apply_weights(p, uu, out=dO)
+        tam.tree_attn_bwd(p, qr, kr, vv, oo, lse, dO, rope_theta=theta, workspace=ws, dq=dqq, dk=dkk, dv=dvv,
+                          status=status)
         comp_done[b].record(stream)
 
     def copy_out(i):
         b = i % 2
-        s_out.wait_event(comp_done[b])
         with torch.cuda.stream(s_out):
-            for dst, src in zip(host_out, outs[b]):
-                dst.copy_(src, non_blocking=True)
+            s_out.wait_event(fwd_done[b])
+            host_out[0].copy_(outs[b][0], non_blocking=True)
+            s_out.wait_event(comp_done[b])
+            for j in (1, 2, 3):
+                host_out[j].copy_(outs[b][j], non_blocking=True)
         out_done[b].record(s_out)
 
     def pipeline(n, e_start=None, e_end=None):
