@@ -211,7 +211,11 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
   for (int i = threadIdx.x; i < ccnt && i < kMaxList; i += blockDim.x) {
     const int qt = gwc ? i : p.col_idx[cp0 + i];
     list_s[i] = qt;
-    lcls_s[i] = gwc ? gw_cls : p.tile_class[(size_t)qt * p.T + kt];
+    // class in bits 0-1, the query tile's node-run count (capped at TREE_MAX_RUNS + 1) in bits 3-7,
+    // so the mask of a partial step reads no global memory
+    lcls_s[i] = gwc ? gw_cls
+                    : static_cast<uint8_t>(p.tile_class[(size_t)qt * p.T + kt] |
+                                           (min(p.tile_nruns[qt], TREE_MAX_RUNS + 1) << 3));
   }
   // step n -> (q head, query tile, class).  Query tiles are walked from the end of the column
   // with the group's q heads innermost, so CTAs running at the same time (whatever their key
@@ -220,7 +224,7 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
     const int gn = srank + n * eff;             // the step's index in the whole column
     const int i = ccnt - 1 - gn / p.grp;
     h = kvh * p.grp + gn % p.grp;
-    if (i < kMaxList) { qt = list_s[i]; cls = lcls_s[i]; }
+    if (i < kMaxList) { qt = list_s[i]; cls = lcls_s[i] & 7; }
     else if (gwc) { qt = i; cls = gw_cls; }
     else { qt = p.col_idx[cp0 + i]; cls = p.tile_class[(size_t)qt * p.T + kt]; }
   };
@@ -504,7 +508,8 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
         vw0 = vw1 = (j < p.gw_len) ? 0xffffffffu : 0u;
       } else if (cls == 1) {
         uint32_t vm[4] = {0u, 0u, 0u, 0u};
-        const int nr = p.tile_nruns[qt];
+        const int gi = ccnt - 1 - (srank + n * eff) / p.grp;   // the step's place in the column
+        const int nr = gi < kMaxList ? static_cast<int>(lcls_s[gi] >> 3) : p.tile_nruns[qt];
         if (nr <= TREE_MAX_RUNS) {
           const int4* runs = reinterpret_cast<const int4*>(aux + C::AUX_RUNS);
           for (int k = 0; k < nr; ++k) {
@@ -536,6 +541,10 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
           tmem_ld16(tmem + lane_off + C::A_COL + 64 * g + 16 * k, *reinterpret_cast<uint32_t(*)[16]>(sv + 16 * k));
 #pragma unroll
         for (int k = 0; k < 4; ++k) tmem_wait_ld16(*reinterpret_cast<uint32_t(*)[16]>(sv + 16 * k));
+        if (cls == 1) {                           // invisible pairs: S = -inf, so P = 2^-inf = 0
+          const uint32_t vw[2] = {vw0, vw1};
+          apply_mask_words<2>(sv, vw, __float_as_uint(-INFINITY));
+        }
         uint32_t pp[32];
 #pragma unroll
         for (int c = 0; c < 64; c += 4) {
@@ -544,14 +553,6 @@ __global__ void __launch_bounds__(BwdCfg<HD>::THREADS, 1)
           f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2x2, f2_pack(l4.x, l4.y)), x0, x1);
           f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), sl2x2, f2_pack(l4.z, l4.w)), x2, x3);
           float pv[4] = {ex2_approx(x0), ex2_approx(x1), ex2_approx(x2), ex2_approx(x3)};
-          if (cls == 1) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int cc = c + e;                 // column inside the group's 64
-              const uint32_t w = cc < 32 ? vw0 : vw1;
-              pv[e] = ((w >> (cc & 31)) & 1u) ? pv[e] : 0.f;
-            }
-          }
 #pragma unroll
           for (int e = 0; e < 4; ++e) pf[c + e] = pv[e];
           pp[c >> 1] = pack_bf16(pv[0], pv[1]);

@@ -448,6 +448,26 @@ DEVI void set_bits_clear_below(uint32_t (&m)[4], int j) {
   }
 }
 
+// v[c] = fill where bit c of the (32 W)-bit mask m is clear.  A mask built from node runs is
+// mostly whole 32-key words of ones or zeros (a run covers whole words, the causal edge cuts one
+// word per row): those words take one test, only a mixed word is selected element by element.
+template <int W, typename T>
+DEVI void apply_mask_words(T (&v)[32 * W], const uint32_t (&m)[W], T fill) {
+#pragma unroll
+  for (int w = 0; w < W; ++w) {
+    const uint32_t b = m[w];
+    if (b == 0xffffffffu) continue;
+    if (b == 0u) {
+#pragma unroll
+      for (int c = 0; c < 32; ++c) v[32 * w + c] = fill;
+    } else {
+#pragma unroll
+      for (int c = 0; c < 32; ++c)
+        if (!((b >> c) & 1u)) v[32 * w + c] = fill;
+    }
+  }
+}
+
 // fp32 RoPE inverse frequency theta^(-2c/d); shared by the forward rotation and the
 // gradient's inverse rotation so that both use the same angles.
 DEVI float rope_inv_freq(int c, int d, float theta) {
