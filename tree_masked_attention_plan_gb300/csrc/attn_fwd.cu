@@ -328,10 +328,21 @@ __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
     float m_ref = 0.f;                         // offset O and l are currently scaled by
     float l_run = 0.f;
     bool ok = true;
+    // node-run count of the tile after the current one, loaded a tile ahead so that a partial
+    // tile's mask does not wait for global memory
+    auto runs_of = [&](int m) -> int {
+      if (m >= cnt) return 0;
+      int kt, cls;
+      row_tile(m, kt, cls);
+      return (GW && (cls & kGwBit)) ? 0 : p.tile_nruns[kt];
+    };
+    int nr_next = runs_of(0);
     for (int n = 0; n < cnt; ++n) {
       const int s = n % C::NS;
       int kt, cls;
       row_tile(n, kt, cls);
+      const int nr_cur = nr_next;
+      nr_next = runs_of(n + 1);
       if (!mbar_wait_warp(&s_full[wg], n & 1, wc)) { ok = false; break; }
       tc_fence_after();
       uint32_t sv[TILE];
@@ -354,7 +365,7 @@ __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
         // the key tile's mask data arrive with its V tile; that stage is refilled only after
         // the last P V of this tile, which waits for this warpgroup's P
         if (!mbar_wait_warp(&v_full[s], (n / C::NS) & 1, wc)) { ok = false; break; }
-        const int nr = p.tile_nruns[kt];
+        const int nr = nr_cur;
         const int jrel = qi - kt * TILE;       // key c is causal-visible iff c <= jrel
         uint32_t vm[4] = {0u, 0u, 0u, 0u};     // bit c: key c visible to this row
         if (nr <= TREE_MAX_RUNS) {             // one ancestor-interval test per node run
