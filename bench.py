@@ -39,8 +39,9 @@ METRIC = "tree-attn fwd+bwd visible-pair TFLOP/s and tokens/s on 1 GB300; % of b
 UNIT = "TFLOP/s"
 DEFAULT_CONFIG = "rollout32k"
 # kernels of this library per step: plan (tokens with per-tile data, classes, lists and orders),
-# RoPE, forward, loss weights, backward (delta and dQ-accumulator zeroing, dK/dV, dQ finalize)
-LAUNCHES_PER_STEP = 3 + 1 + 1 + 1 + 3
+# RoPE, forward, backward (delta with the loss weights g/K folded in, and dQ-accumulator zeroing;
+# dK/dV; dQ finalize)
+LAUNCHES_PER_STEP = 3 + 1 + 1 + 3
 DKDV_PROFILE = os.path.join(ROOT, "profiles", "k_bwd_dkdv_rollout32k.md")
 DKDV_SOURCES = [os.path.join(ROOT, "tree_masked_attention_plan_gb300", "csrc", f) for f in ("attn_bwd.cu", "common.cuh")]
 
@@ -208,7 +209,6 @@ def run_ours(args, rank, world, dev):
     qr, kr = torch.empty_like(q), torch.empty_like(k)
     o = torch.empty_like(q)
     lse = torch.empty(Hq, Np, dtype=torch.float32, device=dev)
-    dO = torch.empty_like(u)
     ws = torch.empty(tam.tree_attn_bwd_workspace(plan, Hq, d), dtype=torch.uint8, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
@@ -223,9 +223,9 @@ def run_ours(args, rank, world, dev):
         ev["fwd"][0].record(stream)
         tam.tree_attn_fwd(p, qr, kr, v, o=o, lse=lse, status=status)
         ev["fwd"][1].record(stream)
-        tam.tree_apply_weights(p, u, out=dO)
-        tam.tree_attn_bwd(p, qr, kr, v, o, lse, dO, rope_theta=theta, workspace=ws, dq=dq, dk=dk, dv=dv,
-                          status=status)
+        # the per-token loss weights g/K are applied inside the backward (no dO pass)
+        tam.tree_attn_bwd_weighted(p, qr, kr, v, o, lse, u, rope_theta=theta, workspace=ws, dq=dq, dk=dk, dv=dv,
+                                   status=status)
 
     def full_step():
         ev["step"][0].record(stream)
@@ -312,8 +312,7 @@ def run_ours(args, rank, world, dev):
         tam.tree_attn_fwd(p, qr, kr, vv, o=oo, lse=lse, status=status)
         fwd_done[b].record(stream)
         stream.wait_event(u_ready[b])
-        tam.tree_apply_weights(p, uu, out=dO)
-        tam.tree_attn_bwd(p, qr, kr, vv, oo, lse, dO, rope_theta=theta, workspace=ws, dq=dqq, dk=dkk, dv=dvv,
+        tam.tree_attn_bwd_weighted(p, qr, kr, vv, oo, lse, uu, rope_theta=theta, workspace=ws, dq=dqq, dk=dkk, dv=dvv,
                           status=status)
         comp_done[b].record(stream)
 
@@ -428,7 +427,7 @@ def run_partitioned(args, dev):
     info = dict(cut_node=int(cut), gateway_tokens=A, parent_tokens=int(len(P["parent"].tokens)),
                 child_tokens=[int(len(c.tokens)) for c in P["children"]])
     return dict(st=st, wl=wl, ms=float(np.mean(ms)), clocks=clk.summary(), info=info,
-                launches=(LAUNCHES_PER_STEP - 1) * (1 + len(P["children"])) + 3)
+                launches=LAUNCHES_PER_STEP * (1 + len(P["children"])) + 3)
 
 
 CONV_METRIC = "tree causal conv1d fwd+bwd algorithmic GB/s on 1 GB300 (hybrid-layer context, section 9.2)"
@@ -807,7 +806,7 @@ def main():
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded tree and N(0,1) bf16 tensors)",
             "config": {"workload": wl.name, "N": st["N"], "paths_K": st["K"], "N_pairs": st["n_pairs"],
                        "N_flat": st["n_flat"], "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d, "rope_theta": wl.theta,
-                       "nonempty_tiles": res["nnz"], "step": "plan+rope+fwd+weights+bwd",
+                       "nonempty_tiles": res["nnz"], "step": "plan+rope+fwd+bwd (loss weights g/K folded into the backward)",
                        "l2": "flushed between steps (256 MiB write, outside the event brackets)",
                        "parallelism": (f"one tree split by kv-head groups over {world} ranks (plan replicated, "
                                        f"no data-path exchange)") if heads else f"one tree per rank x{world}"},

@@ -218,6 +218,21 @@ int tree_attn_bwd(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* 
                   void* workspace, tree_bf16* dq, tree_bf16* dk, tree_bf16* dv,
                   int32_t* status_dev, tree_stream_t stream);
 
+/* tree_attn_bwd for the path-averaged tree loss of "Tree Training 技术详解" section 6.2 / 12,
+ * where dL/dO_t = (g_t / K) U_t: `u` [N][Hq][d] bf16 is the unweighted per-token gradient U and
+ * the plan's weights w_t = g_t / K are applied inside the backward, without forming dO.  The
+ * preprocess takes delta_t = sum_c U_tc O_tc and adds log2(w_t) to the -LSE log2(e) term, so the
+ * probabilities the kernel forms are P w; then dS = (P w)(dP(U) - delta) and
+ * dV = sum (P w)^T U equal the gradients for dO = w U up to rounding (dO = w U is never rounded
+ * to bf16 here, as tree_apply_weights does).  Same arguments, workspace and errors as
+ * tree_attn_bwd (plan without weights -> TREE_ERR_ARG); equivalent to tree_apply_weights
+ * followed by tree_attn_bwd, with one pass over U, O fewer. */
+int tree_attn_bwd_weighted(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k,
+                           const tree_bf16* v, const tree_bf16* o, const float* lse,
+                           const tree_bf16* u, int Hq, int Hkv, int d, float scale,
+                           float rope_theta, void* workspace, tree_bf16* dq, tree_bf16* dk,
+                           tree_bf16* dv, int32_t* status_dev, tree_stream_t stream);
+
 /* Backward of tree_attn_fwd_gateway.  Outputs as tree_attn_bwd for the partition's own tokens
  * (dq then includes the gateway keys' contribution), plus the gateway keys' gradients from
  * this partition's queries: dk_gw, dv_gw fp32 [len][Hkv][d], ADDED to what they hold (the

@@ -92,3 +92,33 @@ def test_bwd_without_rope_inverse():
     back = oracle.rope_transpose(f64(dk2), pos, 10000.0)
     assert np.abs(back - f64(g["dk"])).max() <= 2e-2 * np.abs(f64(g["dk"])).max()
     assert torch.equal(dv2, g["dv"])
+
+
+WEIGHTED = SMALL[:4] + [("caterpillar", None, None, None, None)]
+
+
+@pytest.mark.parametrize("name,tree,Hq,Hkv,d", WEIGHTED, ids=[s[0] for s in WEIGHTED])
+def test_bwd_weighted_matches_oracle_and_unfused(name, tree, Hq, Hkv, d):
+    """tree_attn_bwd_weighted (the weights g_t/K folded into the backward's probabilities, no
+    dO formed) against the fp64 oracle of the path-averaged loss (section 6.2) at the target
+    tolerance, and against tree_apply_weights + tree_attn_bwd: the same sums, where the unfused
+    path rounds dO = w U to bf16 first, so within a few bf16 steps of max |grad|."""
+    wl = make_workload(name) if tree is None else _wl(*tree, Hq, Hkv, d)
+    Hq = wl.Hq
+    heads = [0, 1, 2, 3] if tree is None else range(Hq)
+    t = make_tensors(wl)
+    g = run_gpu(wl.parent, wl.node_len, t)                 # unfused: dO from tree_apply_weights
+    status = tam.new_status()
+    u = t["u"].cuda().contiguous()
+    dq, dk, dv = tam.tree_attn_bwd_weighted(g["plan"], g["qr"], g["kr"], t["v"].cuda(), g["o"], g["lse"], u,
+                                            status=status)
+    torch.cuda.synchronize()
+    tam.check_status(status, "tree_attn_bwd_weighted")
+    fused = dict(dq=dq, dk=dk, dv=dv)
+    ref = oracle_ref(wl.parent, wl.node_len, t, heads=heads, use_nodes=tree is None)
+    e = compare_bwd(fused, ref, heads, Hq, wl.Hkv)
+    diffs = {x: float((f64(fused[x]) - f64(g[x])).__abs__().max() / max(np.abs(f64(g[x])).max(), 1e-30))
+             for x in ("dq", "dk", "dv")}
+    print(f"{name}: fused vs oracle {e}; fused vs unfused {diffs}")
+    assert max(e.values()) <= GRAD_TOL
+    assert max(diffs.values()) <= 2e-2

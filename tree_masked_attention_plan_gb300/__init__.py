@@ -94,6 +94,8 @@ def _lib():
         "tree_attn_bwd_workspace": (ctypes.c_size_t, [P(PlanT), _i32, _i32]),
         "tree_attn_bwd": (_i32, [P(PlanT), _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _f32, _f32, _vp,
                                  _vp, _vp, _vp, _vp, _vp]),
+        "tree_attn_bwd_weighted": (_i32, [P(PlanT), _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _f32, _f32,
+                                          _vp, _vp, _vp, _vp, _vp, _vp]),
         "tree_attn_fwd_gateway": (_i32, [P(PlanT), P(Gateway), _vp, _vp, _vp, _i32, _i32, _i32, _f32, _vp, _vp,
                                          _vp, _vp]),
         "tree_attn_bwd_gateway": (_i32, [P(PlanT), P(Gateway), _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
@@ -310,6 +312,26 @@ def tree_attn_bwd(plan: TreePlan, q, k, v, o, lse, dO, scale=0.0, rope_theta=100
     return dq, dk, dv
 
 
+def tree_attn_bwd_weighted(plan: TreePlan, q, k, v, o, lse, u, scale=0.0, rope_theta=10000.0, workspace=None,
+                           dq=None, dk=None, dv=None, status=None, stream=None):
+    """Backward for dO = w U with the plan's weights w = g/K applied inside (no dO is formed):
+    returns (dq, dk, dv) as tree_attn_bwd(plan, ..., tree_apply_weights(plan, u)) does."""
+    Hq, Hkv, d = _heads(plan, q, k)
+    _need(v, k.shape, torch.bfloat16, "v")
+    _need(o, q.shape, torch.bfloat16, "o")
+    _need(u, q.shape, torch.bfloat16, "u")
+    _need(lse, (Hq, plan.n_pad), torch.float32, "lse")
+    if workspace is None:
+        workspace = torch.empty(tree_attn_bwd_workspace(plan, Hq, d), dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check(_lib().tree_attn_bwd_weighted(plan.ref(), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(u), Hq, Hkv,
+                                         d, float(scale), float(rope_theta), _ptr(workspace), _ptr(dq), _ptr(dk),
+                                         _ptr(dv), _ptr(status), _stream(stream)), "tree_attn_bwd_weighted")
+    return dq, dk, dv
+
+
 def tree_set_timing_events(events):
     """Register torch.cuda.Event objects (up to 4, enable_timing=True) that tree_attn_bwd records
     around its kernels: before delta, before dK/dV, after dK/dV, after dQ finalize.  [] clears."""
@@ -351,7 +373,7 @@ def check_status(status, where="device"):
 
 
 __all__ = ["TreeError", "TreePlan", "tree_plan_query", "tree_plan_nodes", "tree_plan", "tree_rope_fwd", "tree_apply_weights",
-           "tree_attn_fwd", "tree_attn_bwd_workspace", "tree_attn_bwd", "tree_set_wait_limit_ns", "tree_set_bwd_split", "tree_set_fwd_split",
+           "tree_attn_fwd", "tree_attn_bwd_workspace", "tree_attn_bwd", "tree_attn_bwd_weighted", "tree_set_wait_limit_ns", "tree_set_bwd_split", "tree_set_fwd_split",
            "tree_selftest_timeout", "tree_set_timing_events", "new_status", "check_status", "LIB_PATH", "TILE"]
 
 

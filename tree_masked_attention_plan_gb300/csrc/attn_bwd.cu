@@ -118,13 +118,17 @@ DEVI void mbar_wait_drain_b(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
 
 // ------------------------------------------------------------------------------------------
 // per query row: -delta scale (delta_i = sum_c dO_ic O_ic) and -LSE log2e, and zeroes of the
-// same rows of the dQ accumulator.  One block per (32 tokens, q head): 8 threads per token
+// same rows of the dQ accumulator.  With per-token weights w the input is U, dO = w U: delta is
+// then sum_c U_ic O_ic and log2 w_i is added to the -LSE log2e term, which folds the weight into
+// P (P w, exact up to rounding), so that dS = (P w)(dP(U) - delta(U)) and dV = sum (P w)^T U are
+// the gradients for dO without dO being formed.  One block per (32 tokens, q head): 8 threads per token
 // each dot 16 columns (two 16-byte loads of O and of dO, a 256-byte row per token), so the
 // per-head outputs are written as coalesced 128-byte rows.
 template <int HD>
 __global__ void __launch_bounds__(256) k_bwd_pre(const uint4* __restrict__ o, const uint4* __restrict__ dO,
-                                                 const float* __restrict__ lse, float* ndlt, float* nlse2, float scale,
-                                                 float* dqacc, int N, int Npad, int Hq) {
+                                                 const float* __restrict__ lse, const float* __restrict__ w,
+                                                 float* ndlt, float* nlse2, float scale, float* dqacc, int N, int Npad,
+                                                 int Hq) {
   constexpr int TPT = 8, VPT = HD / 8 / TPT;      // threads per token, 16-byte vectors per thread
   const int h = blockIdx.y;
   const int tok = blockIdx.x * 32 + threadIdx.x / TPT;
@@ -145,7 +149,8 @@ __global__ void __launch_bounds__(256) k_bwd_pre(const uint4* __restrict__ o, co
   if (sub == 0 && tok < Npad) {
     const size_t at = (size_t)h * Npad + tok;
     ndlt[at] = tok < N ? -acc * scale : 0.f;
-    nlse2[at] = -lse[at] * 1.4426950408889634f;
+    // with per-token weights (dO = w U, U given): P w = 2^(S scale log2e - LSE log2e + log2 w)
+    nlse2[at] = -lse[at] * 1.4426950408889634f + ((w && tok < N) ? log2f(w[tok]) : 0.f);
   }
   // dQ accumulator rows of these 32 tokens for head h: [HD/4][128][4] block of (h, query tile),
   // 32 consecutive rows = 512 contiguous bytes per 4 columns
@@ -866,9 +871,9 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 template <int HD>
 int launch_bwd(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k, const tree_bf16* v,
-               const tree_bf16* o, const float* lse, const tree_bf16* dO, int Hq, int Hkv, float scale, float theta,
-               void* ws, tree_bf16* dq, tree_bf16* dk, tree_bf16* dv, const tree_gateway_t* gw, float* dk_gw,
-               float* dv_gw, int32_t* status, cudaStream_t s) {
+               const tree_bf16* o, const float* lse, const tree_bf16* dO, const float* w, int Hq, int Hkv, float scale,
+               float theta, void* ws, tree_bf16* dq, tree_bf16* dk, tree_bf16* dv, const tree_gateway_t* gw,
+               float* dk_gw, float* dv_gw, int32_t* status, cudaStream_t s) {
   using C = BwdCfg<HD>;
   const int N = plan->n_tokens, T = plan->n_tiles, Npad = T * TILE;
   float* ndlt = static_cast<float*>(ws);
@@ -900,8 +905,8 @@ int launch_bwd(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k, 
   record_timing_event(0, s);
   {
     k_bwd_pre<HD><<<dim3(Npad / 32, Hq), 256, 0, s>>>(
-        reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dO), lse, ndlt, nlse2, scale, dqacc, N, Npad,
-        Hq);
+        reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dO), lse, w, ndlt, nlse2, scale, dqacc, N,
+        Npad, Hq);
   }
   // CTAs per column: small grids split every column over a cluster (see tree_set_bwd_split)
   const int ctas = (T + G) * Hkv;
@@ -966,8 +971,8 @@ extern "C" size_t tree_attn_bwd_workspace(const tree_plan_t* plan, int Hq, int d
 namespace ta {
 namespace {
 int bwd_entry(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k, const tree_bf16* v,
-              const tree_bf16* o, const float* lse, const tree_bf16* dO, int Hq, int Hkv, int d, float scale,
-              float rope_theta, void* workspace, tree_bf16* dq, tree_bf16* dk, tree_bf16* dv,
+              const tree_bf16* o, const float* lse, const tree_bf16* dO, const float* w, int Hq, int Hkv, int d,
+              float scale, float rope_theta, void* workspace, tree_bf16* dq, tree_bf16* dk, tree_bf16* dv,
               const tree_gateway_t* gw, float* dk_gw, float* dv_gw, int32_t* status_dev, tree_stream_t stream) {
   int rc = plan_ok(plan);
   if (rc) return rc;
@@ -983,9 +988,9 @@ int bwd_entry(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k, c
   if (rc) return rc;
   if (!(scale > 0.f)) scale = 1.f / sqrtf(static_cast<float>(d));
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return d == 128 ? launch_bwd<128>(plan, q, k, v, o, lse, dO, Hq, Hkv, scale, rope_theta, workspace, dq, dk, dv, gw,
-                                    dk_gw, dv_gw, status_dev, s)
-                  : launch_bwd<64>(plan, q, k, v, o, lse, dO, Hq, Hkv, scale, rope_theta, workspace, dq, dk, dv, gw,
+  return d == 128 ? launch_bwd<128>(plan, q, k, v, o, lse, dO, w, Hq, Hkv, scale, rope_theta, workspace, dq, dk, dv,
+                                    gw, dk_gw, dv_gw, status_dev, s)
+                  : launch_bwd<64>(plan, q, k, v, o, lse, dO, w, Hq, Hkv, scale, rope_theta, workspace, dq, dk, dv, gw,
                                    dk_gw, dv_gw, status_dev, s);
 }
 
@@ -1012,8 +1017,18 @@ extern "C" int tree_attn_bwd(const tree_plan_t* plan, const tree_bf16* q, const 
                              const tree_bf16* o, const float* lse, const tree_bf16* dO, int Hq, int Hkv, int d,
                              float scale, float rope_theta, void* workspace, tree_bf16* dq, tree_bf16* dk,
                              tree_bf16* dv, int32_t* status_dev, tree_stream_t stream) {
-  return bwd_entry(plan, q, k, v, o, lse, dO, Hq, Hkv, d, scale, rope_theta, workspace, dq, dk, dv, nullptr, nullptr,
-                   nullptr, status_dev, stream);
+  return bwd_entry(plan, q, k, v, o, lse, dO, nullptr, Hq, Hkv, d, scale, rope_theta, workspace, dq, dk, dv, nullptr,
+                   nullptr, nullptr, status_dev, stream);
+}
+
+extern "C" int tree_attn_bwd_weighted(const tree_plan_t* plan, const tree_bf16* q, const tree_bf16* k,
+                                      const tree_bf16* v, const tree_bf16* o, const float* lse, const tree_bf16* u,
+                                      int Hq, int Hkv, int d, float scale, float rope_theta, void* workspace,
+                                      tree_bf16* dq, tree_bf16* dk, tree_bf16* dv, int32_t* status_dev,
+                                      tree_stream_t stream) {
+  if (!plan || !plan->w) return TREE_ERR_ARG;
+  return bwd_entry(plan, q, k, v, o, lse, u, plan->w, Hq, Hkv, d, scale, rope_theta, workspace, dq, dk, dv, nullptr,
+                   nullptr, nullptr, status_dev, stream);
 }
 
 extern "C" int tree_attn_bwd_gateway(const tree_plan_t* plan, const tree_gateway_t* gw, const tree_bf16* q,
@@ -1022,8 +1037,8 @@ extern "C" int tree_attn_bwd_gateway(const tree_plan_t* plan, const tree_gateway
                                      void* workspace, tree_bf16* dq, tree_bf16* dk, tree_bf16* dv, float* dk_gw,
                                      float* dv_gw, int32_t* status_dev, tree_stream_t stream) {
   if (!gw) return TREE_ERR_ARG;
-  return bwd_entry(plan, q, k, v, o, lse, dO, Hq, Hkv, d, scale, rope_theta, workspace, dq, dk, dv, gw, dk_gw, dv_gw,
-                   status_dev, stream);
+  return bwd_entry(plan, q, k, v, o, lse, dO, nullptr, Hq, Hkv, d, scale, rope_theta, workspace, dq, dk, dv, gw, dk_gw,
+                   dv_gw, status_dev, stream);
 }
 
 extern "C" int tree_relay_add(const int32_t* rows, int32_t len, const float* dk_gw, const float* dv_gw, int Hkv,
