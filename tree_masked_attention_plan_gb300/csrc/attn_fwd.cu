@@ -392,9 +392,9 @@ __global__ void __launch_bounds__(FwdCfg<HD, NH>::THREADS, 1)
       }
       float mx[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) mx[e] = __uint_as_float(sv[e]);
+      for (int e = 0; e < 4; ++e) mx[e] = fmaxf(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1]));
 #pragma unroll
-      for (int c = 4; c < TILE; c += 8)
+      for (int c = 8; c < TILE; c += 8)
 #pragma unroll
         for (int e = 0; e < 4; ++e)
           mx[e] = fmax3(mx[e], __uint_as_float(sv[c + 2 * e]), __uint_as_float(sv[c + 2 * e + 1]));
