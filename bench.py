@@ -212,8 +212,15 @@ def run_ours(args, rank, world, dev):
     ws = torch.empty(tam.tree_attn_bwd_workspace(plan, Hq, d), dtype=torch.uint8, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    ev = {n: [torch.cuda.Event(enable_timing=True) for _ in range(2)] for n in ("step", "fwd", "plan", "rope")}
-    bwd_ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    # one set of events per timed step: the host enqueues step i+1 (its plan's host pass
+    # included) while the GPU runs step i, as a training loop does; the events are read once
+    # after the last step
+    evs = [{n: [torch.cuda.Event(enable_timing=True) for _ in range(2)] for n in ("step", "fwd", "plan", "rope")}
+           for _ in range(max(args.steps, 1))]
+    bwd_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(max(args.steps, 1))]
+    for b in bwd_evs:                          # creates the CUDA events before the timed region
+        tam.tree_set_timing_events(b)
+    ev, bwd_ev = evs[0], bwd_evs[0]
     theta = wl.theta
 
     def step(p):
@@ -248,18 +255,20 @@ def run_ours(args, rank, world, dev):
     torch.cuda.synchronize()
     with ClockSampler(dev.index if dev.index is not None else 0) as clk:
         wall0 = time.perf_counter()
-        for _ in range(args.steps):
+        for i in range(args.steps):
             flush.fill_(1.0)
+            ev, bwd_ev = evs[i], bwd_evs[i]
+            tam.tree_set_timing_events(bwd_ev)
             full_step()
-            torch.cuda.synchronize()
-            times["step"].append(ev["step"][0].elapsed_time(ev["step"][1]))
-            times["fwd"].append(ev["fwd"][0].elapsed_time(ev["fwd"][1]))
-            times["plan"].append(ev["plan"][0].elapsed_time(ev["plan"][1]))
-            times["rope"].append(ev["rope"][0].elapsed_time(ev["rope"][1]))
-            times["bwd"].append(bwd_ev[0].elapsed_time(bwd_ev[3]))
-            times["dkdv"].append(bwd_ev[1].elapsed_time(bwd_ev[2]))
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
+    for e, b in zip(evs[:args.steps], bwd_evs[:args.steps]):
+        times["step"].append(e["step"][0].elapsed_time(e["step"][1]))
+        times["fwd"].append(e["fwd"][0].elapsed_time(e["fwd"][1]))
+        times["plan"].append(e["plan"][0].elapsed_time(e["plan"][1]))
+        times["rope"].append(e["rope"][0].elapsed_time(e["rope"][1]))
+        times["bwd"].append(b[0].elapsed_time(b[3]))
+        times["dkdv"].append(b[1].elapsed_time(b[2]))
     if world > 1:
         torch.distributed.barrier()
     tam.tree_set_timing_events([])
@@ -389,7 +398,6 @@ def run_partitioned(args, dev):
     dv_gw = torch.zeros_like(dk_gw)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
     def step():
         plans = [tam.tree_plan(part.parent, part.node_len, device=dev, pos_offset=part.pos_offset) for part in parts]
@@ -414,15 +422,16 @@ def run_partitioned(args, dev):
         step()
     torch.cuda.synchronize()
     tam.check_status(status, "partitioned warmup")
-    ms = []
+    # per-step events, read after the last step (the host enqueues ahead of the GPU)
+    eps = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     with ClockSampler(dev.index if dev.index is not None else 0) as clk:
-        for _ in range(args.steps):
+        for e0, e1 in eps:
             flush.fill_(1.0)
             e0.record(stream)
             step()
             e1.record(stream)
-            torch.cuda.synchronize()
-            ms.append(e0.elapsed_time(e1))
+        torch.cuda.synchronize()
+    ms = [e0.elapsed_time(e1) for e0, e1 in eps]
     tam.check_status(status, "partitioned steps")
     info = dict(cut_node=int(cut), gateway_tokens=A, parent_tokens=int(len(P["parent"].tokens)),
                 child_tokens=[int(len(c.tokens)) for c in P["children"]])
