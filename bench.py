@@ -19,6 +19,7 @@ cross-entropy fused with the vocabulary projection, TFLOP/s).
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import os
 import subprocess
@@ -122,22 +123,25 @@ def _depth(parent, v):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling every 200 ms while the timed region runs."""
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+    """nvidia-smi clock / throttle sampling every 25 ms; the summary keeps the samples whose
+    timestamps fall inside the timed region (the region of a short run can be under 0.1 s)."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 25
 
     def __init__(self, index):
         self.index = index
         self.proc = None
         self.path = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
         os.close(fd)
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -152,9 +156,12 @@ class ClockSampler:
                 pass
             time.sleep(0.05)
         time.sleep(0.3)
+        self.t0 = time.time()
         return self
 
     def __exit__(self, *a):
+        self.t1 = time.time()
+        time.sleep(2 * self.PERIOD_MS / 1000)     # the sample that covers the region's end
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -163,12 +170,16 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        rows = []
+        rows, stamps = [], []
         try:
             for line in open(self.path):
                 parts = [x.strip() for x in line.split(",")]
-                if len(parts) >= 8:
-                    rows.append(parts)
+                if len(parts) >= 9:
+                    try:
+                        stamps.append(datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp())
+                    except ValueError:
+                        stamps.append(None)
+                    rows.append(parts[1:])
         except OSError:
             pass
         finally:
@@ -176,6 +187,14 @@ class ClockSampler:
                 os.unlink(self.path)
             except OSError:
                 pass
+        if rows and self.t0 is not None and self.t1 is not None:
+            inside = [r for r, t in zip(rows, stamps) if t is not None and self.t0 <= t <= self.t1 + self.PERIOD_MS / 1000]
+            if inside:
+                rows = inside
+            else:                                  # a region shorter than the period: the nearest sample
+                mid = 0.5 * (self.t0 + self.t1)
+                timed = [(abs(t - mid), i) for i, t in enumerate(stamps) if t is not None]
+                rows = [rows[min(timed)[1]]] if timed else rows
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
         sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
