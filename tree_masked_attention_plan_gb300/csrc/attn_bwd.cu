@@ -818,9 +818,23 @@ __global__ void __launch_bounds__(256) k_dq_finalize(const float* __restrict__ d
                                                      __nv_bfloat16* dq, int N, int T, int Hq, int heads_per_block,
                                                      float theta) {
   constexpr int TT = 32, HALF = HD / 2, G = HALF / 8;   // G groups of 8 columns per half row
+  constexpr int PER = (HD / 4) * TT / 256;              // 16-byte loads per thread and head (256 threads)
   __shared__ float s_cos[TT][HALF], s_sin[TT][HALF];
   __shared__ float tile[HD][TT + 1];
   const int i0 = blockIdx.x * TT;
+  const int h0 = blockIdx.y * heads_per_block;
+  // the next head's rows are loaded into registers while the current head is rotated and
+  // stored, so every thread keeps PER loads in flight through the whole block
+  auto load_head = [&](int h, float4 (&v)[PER]) {
+    const float* src = dqacc + ((size_t)h * T + i0 / TILE) * HD * TILE + 4 * (i0 % TILE);
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const int e = threadIdx.x + 256 * k, c4 = e / TT, t = e % TT;
+      v[k] = *reinterpret_cast<const float4*>(src + ((size_t)c4 * TILE + t) * 4);
+    }
+  };
+  float4 nxt[PER];
+  load_head(h0, nxt);                                   // in flight during the angle table
   for (int e = threadIdx.x; e < TT * HALF; e += blockDim.x) {
     const int t = e / HALF, c = e % HALF;
     const int i = i0 + t;
@@ -830,19 +844,18 @@ __global__ void __launch_bounds__(256) k_dq_finalize(const float* __restrict__ d
     s_sin[t][c] = sv;
   }
   const int t_out = threadIdx.x / G, g_out = threadIdx.x % G;
-  const int h0 = blockIdx.y * heads_per_block;
   for (int h = h0; h < h0 + heads_per_block; ++h) {
     __syncthreads();
-    const float* src = dqacc + ((size_t)h * T + i0 / TILE) * HD * TILE + 4 * (i0 % TILE);
-    for (int e = threadIdx.x; e < (HD / 4) * TT; e += blockDim.x) {
-      const int c4 = e / TT, t = e % TT;
-      const float4 v = *reinterpret_cast<const float4*>(src + ((size_t)c4 * TILE + t) * 4);
-      tile[4 * c4 + 0][t] = v.x;
-      tile[4 * c4 + 1][t] = v.y;
-      tile[4 * c4 + 2][t] = v.z;
-      tile[4 * c4 + 3][t] = v.w;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const int e = threadIdx.x + 256 * k, c4 = e / TT, t = e % TT;
+      tile[4 * c4 + 0][t] = nxt[k].x;
+      tile[4 * c4 + 1][t] = nxt[k].y;
+      tile[4 * c4 + 2][t] = nxt[k].z;
+      tile[4 * c4 + 3][t] = nxt[k].w;
     }
     __syncthreads();
+    if (h + 1 < h0 + heads_per_block) load_head(h + 1, nxt);
     const int i = i0 + t_out;
     if (t_out < TT && i < N) {
       uint32_t lo[4], hi[4];
